@@ -1,0 +1,198 @@
+"""Plain CPU oracle for the TBE hot path (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library itself never does, and
+the two share no code: the oracle is ``tbe_oracle.c``, built with gcc into
+``liboracle_tbe.so`` and called through ctypes on numpy arrays.
+
+Every function here is a thin marshalling wrapper; the arithmetic and its
+citations are in ``tbe_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tbe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_tbe.so")
+_lib = None
+
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32, i64, f32, f64, u16 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                   ctypes.c_double, ctypes.c_uint16)
+        L.tbe_oracle_forward.restype = i64
+        L.tbe_oracle_forward.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P]
+        L.tbe_oracle_preprocess.restype = i64
+        L.tbe_oracle_preprocess.argtypes = [i32, i64, P, P, P, i64, P, P, P, P, P, P]
+        L.tbe_oracle_backward_adagrad.restype = i64
+        L.tbe_oracle_backward_adagrad.argtypes = [i32, i64, i32, i32, P, P, P, P, P, i64, P, P, P,
+                                                  f32, f32, P, P]
+        L.tbe_oracle_rows_update.restype = i64
+        L.tbe_oracle_rows_update.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, f32, f32, P, i64,
+                                             P, P, P, P]
+        L.tbe_oracle_histogram.restype = i64
+        L.tbe_oracle_histogram.argtypes = [i32, i64, i32, P, P, P, P]
+        for n in ("tbe_oracle_to_half", "tbe_oracle_to_bf16"):
+            getattr(L, n).restype = u16
+            getattr(L, n).argtypes = [f64]
+        for n in ("tbe_oracle_from_half", "tbe_oracle_from_bf16"):
+            getattr(L, n).restype = f64
+            getattr(L, n).argtypes = [u16]
+        _lib = L
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _wbits(W: np.ndarray, dtype: str) -> np.ndarray:
+    """Weights as raw storage: float32 array for f32, uint16 bit patterns for f16/bf16."""
+    if dtype == "f32":
+        return np.ascontiguousarray(W, dtype=np.float32)
+    assert W.dtype == np.uint16, "f16/bf16 weights are passed as uint16 bit patterns"
+    return np.ascontiguousarray(W)
+
+
+def forward(wl, W: np.ndarray, bags: Optional[np.ndarray] = None, want_abs: bool = False):
+    """Pooled forward.  Returns (out, abs_sum|None, oob, bad_bags).
+
+    ``W`` is the flat [rows_total, D] table store (float32, or uint16 bits for
+    f16/bf16).  With ``bags`` (int64 bag ids t*B+b) out is [len(bags), D].
+    """
+    L = lib()
+    W = _wbits(W, wl.dtype)
+    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+    idx = _c(wl.indices, np.int32)
+    off = _c(wl.offsets, np.int32)
+    psw = _c(wl.per_sample_weights, np.float32)
+    wt = _c(wl.weighted_tables, np.uint8)
+    if bags is None:
+        out = np.zeros((wl.B, wl.T * wl.D), dtype=np.float32)
+        nb = 0
+    else:
+        bags = np.ascontiguousarray(bags, dtype=np.int64)
+        out = np.zeros((len(bags), wl.D), dtype=np.float32)
+        nb = len(bags)
+    ab = np.zeros(out.shape, dtype=np.float64) if want_abs else None
+    bad = ctypes.c_int64(0)
+    oob = L.tbe_oracle_forward(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(to), _p(idx),
+                               _p(off), _p(psw), _p(wt), _p(bags), nb, _p(out), _p(ab),
+                               ctypes.addressof(bad))
+    return out, ab, int(oob), int(bad.value)
+
+
+def preprocess(wl):
+    """Batch inversion.  Returns dict of sorted_keys, sorted_pos, unique_keys,
+    run_len, seg_off (int64) and num_unique, n_valid."""
+    L = lib()
+    N = wl.N
+    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+    sk = np.zeros(max(N, 1), np.int64)
+    sp = np.zeros(max(N, 1), np.int64)
+    uk = np.zeros(max(N, 1), np.int64)
+    rl = np.zeros(max(N, 1), np.int64)
+    so = np.zeros(N + 1, np.int64)
+    nv = ctypes.c_int64(0)
+    U = L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(_c(wl.indices, np.int32)),
+                                _p(_c(wl.offsets, np.int32)), N, _p(sk), _p(sp), _p(uk), _p(rl),
+                                _p(so), ctypes.addressof(nv))
+    nv = int(nv.value)
+    return dict(sorted_keys=sk[:nv], sorted_pos=sp[:nv], unique_keys=uk[:U], run_len=rl[:U],
+                seg_off=so[:U + 1], num_unique=int(U), n_valid=nv)
+
+
+def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarray,
+                     want_row_grad: bool = False, want_update_count: bool = False):
+    """Backward + exact rowwise Adagrad, in place on copies.
+
+    Returns (W_new, momentum_new, U, row_grad|None, update_count|None).
+    """
+    L = lib()
+    W = _wbits(W, wl.dtype).copy()
+    m = np.ascontiguousarray(momentum, dtype=np.float32).copy()
+    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+    go = np.ascontiguousarray(grad_out, dtype=np.float32)
+    rg = np.zeros((wl.rows_total, wl.D), np.float64) if want_row_grad else None
+    uc = np.zeros(wl.rows_total, np.int32) if want_update_count else None
+    U = L.tbe_oracle_backward_adagrad(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(m), _p(to),
+                                      _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)),
+                                      wl.N, _p(_c(wl.per_sample_weights, np.float32)),
+                                      _p(_c(wl.weighted_tables, np.uint8)), _p(go),
+                                      float(wl.lr), float(wl.eps), _p(rg), _p(uc))
+    return W, m, int(U), rg, uc
+
+
+def rows_update(wl, rows: np.ndarray, W_rows: np.ndarray, mom_rows: np.ndarray,
+                grad_out: np.ndarray):
+    """Sampled-row backward: rows (sorted distinct linearised keys) with their
+    pre-update W rows and momentum.  Returns (W_rows_new, mom_new, row_grad, counts, n_valid)."""
+    L = lib()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert np.all(np.diff(rows) > 0)
+    k = len(rows)
+    Wr = _wbits(W_rows, wl.dtype).copy()
+    mr = np.ascontiguousarray(mom_rows, dtype=np.float32).copy()
+    rg = np.zeros((k, wl.D), np.float64)
+    cnt = np.zeros(k, np.int64)
+    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+    nv = L.tbe_oracle_rows_update(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(to),
+                                  _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)),
+                                  _p(_c(wl.per_sample_weights, np.float32)),
+                                  _p(_c(wl.weighted_tables, np.uint8)),
+                                  _p(np.ascontiguousarray(grad_out, dtype=np.float32)),
+                                  float(wl.lr), float(wl.eps), _p(rows), k, _p(Wr), _p(mr),
+                                  _p(rg), _p(cnt))
+    return Wr, mr, rg, cnt, int(nv)
+
+
+def histogram(wl, Emax: int = 64) -> np.ndarray:
+    """Per-bag row counts, int32 [T, B, Emax]."""
+    L = lib()
+    c = np.zeros((wl.T, wl.B, Emax), np.int32)
+    L.tbe_oracle_histogram(wl.T, wl.B, Emax, _p(np.ascontiguousarray(wl.table_offset, np.int64)),
+                           _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)), _p(c))
+    return c
+
+
+def to_half_bits(x: float) -> int:
+    return int(lib().tbe_oracle_to_half(float(x)))
+
+
+def to_bf16_bits(x: float) -> int:
+    return int(lib().tbe_oracle_to_bf16(float(x)))
+
+
+def from_half_bits(h: int) -> float:
+    return float(lib().tbe_oracle_from_half(int(h)))
+
+
+def from_bf16_bits(h: int) -> float:
+    return float(lib().tbe_oracle_from_bf16(int(h)))

@@ -1,0 +1,464 @@
+/*
+ * Plain CPU oracle for the table-batched embedding (TBE) hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library calls or links this
+ * file; only the tests, the package's smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or helper with the CUDA path.
+ *
+ * What it computes (sources are the pages' sections, by page title):
+ *
+ *  - Forward pooled sum over KeyedJagged CSR input.  FBTriton TBE redesign
+ *    (accesspath.com), "Backward kernels", problem statement and notation
+ *    (T, E, D, L, B); TorchEasyRec analysis (39.107.221.112 article 1724244),
+ *    section 1 "KeyedJaggedTensor" (all ids concatenated, one length per
+ *    sample per feature, one fused lookup for all features).
+ *  - Per-sample weights: FBTriton TBE redesign, "Backward kernels",
+ *    weighted-tables paragraph (each gradient row is scaled by its per-sample
+ *    weight before accumulation); the forward is read as the matching
+ *    weighted pooled sum.
+ *  - Batch inversion: FBTriton TBE redesign, "transpose_embedding_input"
+ *    (linearise (table,row), sort, run-length encode into runs of one unique
+ *    row with all positions touching it) and decision checklist item 6
+ *    (int32 keys when the linearised range is below 2^31).
+ *  - Backward: FBTriton TBE redesign, "Backward kernels": for every unique
+ *    (table,row) touched by the batch, sum the upstream gradient rows of all
+ *    positions touching it, then apply exactly one optimizer update to that
+ *    row.
+ *  - Optimizer: exact rowwise Adagrad (named in FBTriton TBE redesign,
+ *    "Forward state reuse and preprocessing"):
+ *        m[r] += mean_d(g[r,d]^2);  w[r,d] -= lr * g[r,d] / (sqrt(m[r]) + eps)
+ *    with the updated m in the denominator, eps outside the square root.
+ *  - Small-table histogram: FBTriton TBE redesign, "Forward state reuse and
+ *    preprocessing" (forward histogram counts saved for backward) and
+ *    decision checklist item 2 (E<=64, 64<=D<=128, L>=64, FP16, unweighted).
+ *    The histogram path computes the same values as the generic path; the
+ *    oracle for it is the generic definition plus the plain count function
+ *    below.
+ *
+ * Arithmetic: every sum is accumulated in double, and every stored result is
+ * rounded once from double to its stored type (float32 outputs and momentum;
+ * the table dtype for weights, round-to-nearest-even).  The pages fix the
+ * kernel's accumulation precision (decision checklist item 1: FP32 for
+ * FP16/BF16 weights, FP64 for FP32 weights); the oracle is at least as
+ * accurate as either, so a comparison measures the kernel's own rounding.
+ *
+ * Out-of-range indices (idx < 0 or idx >= E_t) are counted, contribute
+ * nothing to the forward and take no part in the backward.  A bag whose end
+ * offset is below its start is counted as malformed and treated as empty.
+ *
+ * Dtype codes: 0 = float32, 1 = float16, 2 = bfloat16.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* Stored-type conversions, written from the IEEE 754 binary16 and the  */
+/* bfloat16 (float32 with the low 16 bits dropped) encodings.           */
+
+static double half_bits_to_double(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 1024), e - 25);     /* 1.m * 2^(e-15) */
+    return s ? -v : v;
+}
+
+/* nearest binary16, ties to even (nearbyint in the default rounding mode) */
+static uint16_t double_to_half_bits(double x)
+{
+    uint16_t s = signbit(x) ? 0x8000 : 0;
+    if (isnan(x))
+        return 0x7E00;
+    double a = fabs(x);
+    if (isinf(a))
+        return s | 0x7C00;
+    if (a < ldexp(1.0, -14)) {                     /* subnormal quantum 2^-24 */
+        double q = nearbyint(ldexp(a, 24));        /* q == 1024 is the smallest normal */
+        return s | (uint16_t)q;
+    }
+    int e;
+    frexp(a, &e);                                  /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    double q = nearbyint(ldexp(a, 10 - E));        /* significand in [1024, 2048] */
+    if (q == 2048.0) {
+        q = 1024.0;
+        E += 1;
+    }
+    if (E > 15)
+        return s | 0x7C00;
+    return s | (uint16_t)((E + 15) << 10) | (uint16_t)((int)q - 1024);
+}
+
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* nearest bfloat16 (8-bit exponent, 7 stored significand bits), ties to even */
+static uint16_t double_to_bf16_bits(double x)
+{
+    uint16_t s = signbit(x) ? 0x8000 : 0;
+    if (isnan(x))
+        return s | 0x7FC0;
+    double a = fabs(x);
+    if (isinf(a))
+        return s | 0x7F80;
+    if (a < ldexp(1.0, -126)) {                    /* subnormal quantum 2^-133 */
+        double q = nearbyint(ldexp(a, 133));       /* q == 128 is the smallest normal */
+        return s | (uint16_t)q;
+    }
+    int e;
+    frexp(a, &e);
+    int E = e - 1;
+    double q = nearbyint(ldexp(a, 7 - E));         /* significand in [128, 256] */
+    if (q == 256.0) {
+        q = 128.0;
+        E += 1;
+    }
+    if (E > 127)
+        return s | 0x7F80;
+    return s | (uint16_t)((E + 127) << 7) | (uint16_t)((int)q - 128);
+}
+
+static double load_w(const void *W, int dtype, int64_t i)
+{
+    if (dtype == 0)
+        return (double)((const float *)W)[i];
+    if (dtype == 1)
+        return half_bits_to_double(((const uint16_t *)W)[i]);
+    return bf16_bits_to_double(((const uint16_t *)W)[i]);
+}
+
+static void store_w(void *W, int dtype, int64_t i, double v)
+{
+    if (dtype == 0)
+        ((float *)W)[i] = (float)v;
+    else if (dtype == 1)
+        ((uint16_t *)W)[i] = double_to_half_bits(v);
+    else
+        ((uint16_t *)W)[i] = double_to_bf16_bits(v);
+}
+
+/* exported for the conversion pins */
+uint16_t tbe_oracle_to_half(double x) { return double_to_half_bits(x); }
+uint16_t tbe_oracle_to_bf16(double x) { return double_to_bf16_bits(x); }
+double tbe_oracle_from_half(uint16_t h) { return half_bits_to_double(h); }
+double tbe_oracle_from_bf16(uint16_t h) { return bf16_bits_to_double(h); }
+
+/* ------------------------------------------------------------------ */
+
+static double sample_weight(const float *psw, const uint8_t *weighted, int64_t t, int64_t p)
+{
+    if (psw == NULL)
+        return 1.0;
+    if (weighted != NULL && !weighted[t])
+        return 1.0;
+    return (double)psw[p];
+}
+
+/*
+ * Forward pooled sum for a list of bags (all T*B bags when bags == NULL).
+ *
+ *   out[b, t*D + d] = sum_{p in bag (t,b), 0 <= idx_p < E_t} w_p * W[table_offset[t] + idx_p, d]
+ *
+ * With bags == NULL the output is the full [B, T*D] matrix; with a bag list
+ * row k of out ([nbags, D]) belongs to bag bags[k] = t*B + b.
+ * abs_sum (nullable) receives sum |w_p * W[.., d]| in the same layout: the
+ * scale that bounds any summation-order rounding of out.
+ * Returns the number of out-of-range lookups in the bags visited;
+ * *bad_bags (nullable) the number of bags with end < start.
+ */
+int64_t tbe_oracle_forward(int32_t T, int64_t B, int32_t D, int32_t dtype, const void *W,
+                           const int64_t *table_offset, const int32_t *indices,
+                           const int32_t *offsets, const float *psw, const uint8_t *weighted,
+                           const int64_t *bags, int64_t nbags, float *out, double *abs_sum,
+                           int64_t *bad_bags)
+{
+    int64_t oob = 0, bad = 0;
+    int64_t n = bags ? nbags : (int64_t)T * B;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)D);
+    double *aab = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int64_t k = 0; k < n; ++k) {
+        int64_t bag = bags ? bags[k] : k;
+        int64_t t = bag / B, b = bag % B;
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        for (int d = 0; d < D; ++d)
+            acc[d] = aab[d] = 0.0;
+        int64_t start = offsets[bag], end = offsets[bag + 1];
+        if (end < start)
+            ++bad;
+        for (int64_t p = start; p < end; ++p) {
+            int64_t idx = indices[p];
+            if (idx < 0 || idx >= E) {
+                ++oob;
+                continue;
+            }
+            double w = sample_weight(psw, weighted, t, p);
+            int64_t row = table_offset[t] + idx;
+            for (int d = 0; d < D; ++d) {
+                double v = w * load_w(W, dtype, row * D + d);
+                acc[d] += v;
+                aab[d] += fabs(v);
+            }
+        }
+        int64_t o = bags ? k * D : (b * T + t) * D;
+        for (int d = 0; d < D; ++d) {
+            out[o + d] = (float)acc[d];
+            if (abs_sum)
+                abs_sum[o + d] = aab[d];
+        }
+    }
+    free(acc);
+    free(aab);
+    if (bad_bags)
+        *bad_bags = bad;
+    return oob;
+}
+
+/* ------------------------------------------------------------------ */
+/* Batch inversion: linearise, stable sort, run-length encode.          */
+
+typedef struct {
+    int64_t key;
+    int64_t pos;
+} kp_t;
+
+static int cmp_key_pos(const void *a, const void *b)
+{
+    const kp_t *x = (const kp_t *)a, *y = (const kp_t *)b;
+    if (x->key != y->key)
+        return x->key < y->key ? -1 : 1;
+    if (x->pos != y->pos)
+        return x->pos < y->pos ? -1 : 1;
+    return 0;
+}
+
+/* bag id (t*B + b) of every position p; -1 for positions in no bag */
+static int64_t *bag_of_positions(int32_t T, int64_t B, const int32_t *offsets, int64_t N)
+{
+    int64_t *bag = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    for (int64_t p = 0; p < N; ++p)
+        bag[p] = -1;
+    for (int64_t g = 0; g < (int64_t)T * B; ++g)
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p)
+            if (p >= 0 && p < N)
+                bag[p] = g;
+    return bag;
+}
+
+/*
+ * key_p = table_offset[t] + idx_p for every in-range lookup p (t its table),
+ * sorted by (key, p) -- a stable sort by key -- then run-length encoded:
+ *   unique_keys[r], run_len[r], seg_off[r] (exclusive prefix sum of run_len,
+ *   seg_off[U] = N' = number of in-range lookups).
+ * sorted_keys/sorted_pos have N' entries.  Any output may be NULL.
+ * Returns U.
+ */
+int64_t tbe_oracle_preprocess(int32_t T, int64_t B, const int64_t *table_offset,
+                              const int32_t *indices, const int32_t *offsets, int64_t N,
+                              int64_t *sorted_keys, int64_t *sorted_pos, int64_t *unique_keys,
+                              int64_t *run_len, int64_t *seg_off, int64_t *n_valid)
+{
+    int64_t *bag = bag_of_positions(T, B, offsets, N);
+    kp_t *kp = (kp_t *)malloc(sizeof(kp_t) * (size_t)(N > 0 ? N : 1));
+    int64_t nv = 0;
+    for (int64_t p = 0; p < N; ++p) {
+        if (bag[p] < 0)
+            continue;
+        int64_t t = bag[p] / B;
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        int64_t idx = indices[p];
+        if (idx < 0 || idx >= E)
+            continue;
+        kp[nv].key = table_offset[t] + idx;
+        kp[nv].pos = p;
+        ++nv;
+    }
+    qsort(kp, (size_t)nv, sizeof(kp_t), cmp_key_pos);
+    int64_t U = 0;
+    for (int64_t i = 0; i < nv; ++i) {
+        if (sorted_keys)
+            sorted_keys[i] = kp[i].key;
+        if (sorted_pos)
+            sorted_pos[i] = kp[i].pos;
+        if (i == 0 || kp[i].key != kp[i - 1].key) {
+            if (unique_keys)
+                unique_keys[U] = kp[i].key;
+            if (seg_off)
+                seg_off[U] = i;
+            ++U;
+        }
+        if (run_len)
+            run_len[U - 1] = (i == 0 || kp[i].key != kp[i - 1].key) ? 1 : run_len[U - 1] + 1;
+    }
+    if (seg_off)
+        seg_off[U] = nv;
+    if (n_valid)
+        *n_valid = nv;
+    free(kp);
+    free(bag);
+    return U;
+}
+
+/* ------------------------------------------------------------------ */
+/* Backward with the fused exact rowwise Adagrad update.                 */
+
+/* One exact rowwise Adagrad step on row `row` with row gradient g[0..D). */
+static void adagrad_row(void *W, float *momentum, int32_t D, int32_t dtype, int64_t row,
+                        const double *g, float lr, float eps)
+{
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d)
+        ss += g[d] * g[d];
+    momentum[row] = (float)((double)momentum[row] + ss / (double)D);
+    double den = sqrt((double)momentum[row]) + (double)eps;
+    for (int d = 0; d < D; ++d) {
+        double w = load_w(W, dtype, row * D + d);
+        store_w(W, dtype, row * D + d, w - (double)lr * g[d] / den);
+    }
+}
+
+/*
+ * Full backward in the pages' order: batch inversion (linearise, stable
+ * sort, RLE), then for every run r (one unique row) the row gradient
+ *     g[d] = sum_{p in run r, sorted order} w_p * grad_out[b(p), t*D + d]
+ * and exactly one Adagrad update of that row.  W and momentum are updated in
+ * place; rows no in-range lookup touches are not written.
+ * row_grad (nullable, [rows_total, D]) receives g of every touched row;
+ * update_count (nullable, [rows_total]) counts updates applied per row.
+ * Returns U, the number of rows updated.
+ */
+int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dtype, void *W,
+                                    float *momentum, const int64_t *table_offset,
+                                    const int32_t *indices, const int32_t *offsets, int64_t N,
+                                    const float *psw, const uint8_t *weighted,
+                                    const float *grad_out, float lr, float eps,
+                                    double *row_grad, int32_t *update_count)
+{
+    int64_t *skeys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    int64_t *spos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    int64_t *ukeys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    int64_t *soff = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N + 1));
+    int64_t U = tbe_oracle_preprocess(T, B, table_offset, indices, offsets, N, skeys, spos, ukeys,
+                                      NULL, soff, NULL);
+    int64_t *bag = bag_of_positions(T, B, offsets, N);
+    double *g = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int64_t r = 0; r < U; ++r) {
+        int64_t row = ukeys[r];
+        for (int d = 0; d < D; ++d)
+            g[d] = 0.0;
+        for (int64_t i = soff[r]; i < soff[r + 1]; ++i) {
+            int64_t p = spos[i];
+            int64_t t = bag[p] / B, b = bag[p] % B;
+            double w = sample_weight(psw, weighted, t, p);
+            const float *grow = grad_out + (b * T + t) * D;
+            for (int d = 0; d < D; ++d)
+                g[d] += w * (double)grow[d];
+        }
+        if (row_grad)
+            for (int d = 0; d < D; ++d)
+                row_grad[row * D + d] = g[d];
+        adagrad_row(W, momentum, D, dtype, row, g, lr, eps);
+        if (update_count)
+            update_count[row] += 1;
+    }
+    free(g);
+    free(bag);
+    free(soff);
+    free(ukeys);
+    free(spos);
+    free(skeys);
+    return U;
+}
+
+/* ------------------------------------------------------------------ */
+/* Sampled rows, for full-size checks.                                   */
+
+static int cmp_i64(const void *a, const void *b)
+{
+    int64_t x = *(const int64_t *)a, y = *(const int64_t *)b;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/*
+ * For k sampled linearised rows (sorted ascending, distinct) compute by one
+ * scan over all lookups their lookup count, row gradient (summed in position
+ * order, double) and the Adagrad result.  W_rows (dtype, [k, D]) and
+ * mom_rows ([k]) hold the rows' values before the update and are updated in
+ * place; rows with count 0 are left untouched.  row_grad ([k, D]) and counts
+ * ([k]) are outputs.  Returns the number of in-range lookups scanned.
+ */
+int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
+                               const int64_t *table_offset, const int32_t *indices,
+                               const int32_t *offsets, const float *psw, const uint8_t *weighted,
+                               const float *grad_out, float lr, float eps, const int64_t *rows,
+                               int64_t k, void *W_rows, float *mom_rows, double *row_grad,
+                               int64_t *counts)
+{
+    int64_t nv = 0;
+    for (int64_t i = 0; i < k * D; ++i)
+        row_grad[i] = 0.0;
+    for (int64_t i = 0; i < k; ++i)
+        counts[i] = 0;
+    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
+        int64_t t = g / B, b = g % B;
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
+            int64_t idx = indices[p];
+            if (idx < 0 || idx >= E)
+                continue;
+            ++nv;
+            int64_t key = table_offset[t] + idx;
+            const int64_t *hit = (const int64_t *)bsearch(&key, rows, (size_t)k, sizeof(int64_t), cmp_i64);
+            if (!hit)
+                continue;
+            int64_t s = hit - rows;
+            double w = sample_weight(psw, weighted, t, p);
+            const float *grow = grad_out + (b * T + t) * D;
+            for (int d = 0; d < D; ++d)
+                row_grad[s * D + d] += w * (double)grow[d];
+            counts[s] += 1;
+        }
+    }
+    for (int64_t s = 0; s < k; ++s)
+        if (counts[s] > 0)
+            adagrad_row(W_rows, mom_rows, D, dtype, s, row_grad + s * D, lr, eps);
+    return nv;
+}
+
+/* ------------------------------------------------------------------ */
+/* Small-table histogram counts.                                         */
+
+/*
+ * counts[(t*B + b)*Emax + e] = #{p in bag (t,b) : idx_p == e}, for
+ * 0 <= e < E_t (out-of-range lookups are not counted).  Emax >= every E_t.
+ * Returns the number of lookups counted.
+ */
+int64_t tbe_oracle_histogram(int32_t T, int64_t B, int32_t Emax, const int64_t *table_offset,
+                             const int32_t *indices, const int32_t *offsets, int32_t *counts)
+{
+    int64_t total = 0;
+    memset(counts, 0, sizeof(int32_t) * (size_t)T * (size_t)B * (size_t)Emax);
+    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
+        int64_t t = g / B;
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
+            int64_t idx = indices[p];
+            if (idx < 0 || idx >= E)
+                continue;
+            counts[g * Emax + idx] += 1;
+            ++total;
+        }
+    }
+    return total;
+}
