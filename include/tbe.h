@@ -1,0 +1,242 @@
+/*
+ * tbe.h -- C ABI of the GB300 table-batched embedding (TBE) training hot path.
+ *
+ * The operation (FBTriton TBE redesign, accesspath.com, section "Backward
+ * kernels: three paths by segment length", notation paragraph): T embedding
+ * tables, table t with E_t rows of D elements; a batch of B bags per table,
+ * bag (t,b) holding L_(t,b) row indices (L is the pooling factor).  Input is
+ * KeyedJagged CSR (TorchEasyRec analysis, 39.107.221.112 article 1724244,
+ * section 1 "KeyedJaggedTensor"): one `indices` array with every lookup of
+ * every table concatenated, and `offsets[T*B+1]`, bag (t,b) being
+ * indices[offsets[t*B+b] .. offsets[t*B+b+1]).  Tables are key-major: all
+ * bags of table 0, then all bags of table 1, ...
+ *
+ *   forward:    out[b, t*D + d] = sum_{p in bag (t,b)} w_p * W_t[idx_p, d]
+ *   backward:   for each unique (t,row) touched by the batch,
+ *               g[d] = sum_{p touching it} w_p * grad_out[b(p), t*D + d],
+ *               then exactly one exact-rowwise-Adagrad update of that row:
+ *               m[row] += mean_d g[d]^2;  W[row,d] -= lr*g[d]/(sqrt(m[row])+eps)
+ *
+ * w_p is the per-sample weight (1 on unweighted tables).
+ *
+ * Conventions for every entry point
+ *  - Ownership: the caller allocates and owns every buffer.  The library
+ *    allocates nothing, frees nothing and keeps no global state; all
+ *    scratch memory comes from the caller's `workspace`.
+ *  - Pointers named device are device memory; those named host are host
+ *    memory read synchronously during the call.
+ *  - Streams: every device operation is enqueued on `stream`; the calls
+ *    return before the work completes and never synchronise the host.
+ *  - Errors found on the host (null or misaligned pointers, unsupported
+ *    sizes, too-small buffers) return a non-zero tbe_status before anything
+ *    is enqueued.  Errors that depend on the data are reported in the
+ *    caller's device status words (`dev_status`, TBE_STATUS_WORDS int32),
+ *    to be read after the stream completes:
+ *        dev_status[0]  += number of out-of-range indices seen by tbe_forward
+ *                          (tbe_preprocess skips them without counting)
+ *        dev_status[1]  |= TBE_FLAG_* bits
+ *    The caller zeroes dev_status when it wants a fresh count.  No kernel
+ *    traps, asserts or waits without bound.
+ *  - Threading: the functions are reentrant; calls on different streams
+ *    must use different workspace and meta buffers.
+ */
+#ifndef TBE_GB300_TBE_H
+#define TBE_GB300_TBE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tbe_status {
+    TBE_OK = 0,
+    TBE_ERR_NULL_POINTER = 1,       /* a required pointer is NULL */
+    TBE_ERR_INVALID_ARGUMENT = 2,   /* T, B, N, D out of range, table_offset not monotone, ... */
+    TBE_ERR_UNSUPPORTED_DIM = 3,    /* D*sizeof(weight) not one of the supported row sizes */
+    TBE_ERR_UNSUPPORTED_DTYPE = 4,
+    TBE_ERR_MISALIGNED = 5,         /* a device pointer is not 16-byte aligned */
+    TBE_ERR_KEY_RANGE = 6,          /* sum of E_t (+1 sentinel) does not fit int32 keys */
+    TBE_ERR_BUFFER_TOO_SMALL = 7,   /* workspace or meta smaller than tbe_query_sizes says */
+    TBE_ERR_META = 8,               /* meta not bound, or bound for another problem */
+    TBE_ERR_HISTOGRAM_SHAPE = 9,    /* histogram path forced on a shape it does not cover */
+    TBE_ERR_CUDA = 10               /* a kernel launch failed (see cudaGetLastError) */
+} tbe_status;
+
+typedef enum tbe_dtype { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
+
+/* dev_status[1] bits */
+#define TBE_FLAG_BAD_OFFSETS   0x1  /* a bag with offsets[g+1] < offsets[g]; treated as empty */
+#define TBE_FLAG_FP16_OVERFLOW 0x2  /* |grad| > 65504 in the histogram path's FP16 hi/lo split */
+#define TBE_FLAG_SORT_TIMEOUT  0x4  /* radix-sort look-back gave up waiting: sort output invalid */
+#define TBE_FLAG_HIST_COUNT    0x8  /* a histogram count exceeded 2048 (not exact in FP16) */
+#define TBE_FLAG_MMA_TIMEOUT   0x10 /* a tensor-core completion wait gave up: output invalid */
+#define TBE_STATUS_WORDS 4
+
+/* Where runs with SL >= sl_threshold are reduced (FBTriton TBE redesign,
+ * "Backward kernels", paths 2 and 3). */
+typedef enum tbe_long_run_mode {
+    TBE_LONG_AUTO = 0,       /* = TBE_LONG_FUSED on this GPU */
+    TBE_LONG_TWO_KERNEL = 1, /* grad_accum into the workspace + a separate apply kernel */
+    TBE_LONG_FUSED = 2       /* one launch; the last-arriving chunk applies the update */
+} tbe_long_run_mode;
+
+/* Small-table histogram path (FBTriton TBE redesign, "Forward state reuse
+ * and preprocessing" and decision checklist item 2). */
+typedef enum tbe_hist_mode {
+    TBE_HIST_AUTO = 0,   /* used when E_t <= 64, 64 <= D <= 128, D % 16 == 0, FP16
+                            weights, no per-sample weights and N >= 64*T*B */
+    TBE_HIST_OFF = 1,    /* always the generic gather path */
+    TBE_HIST_FORCE = 2   /* histogram path whenever the shape is covered (any L) */
+} tbe_hist_mode;
+
+typedef struct tbe_config {
+    int32_t sl_threshold;    /* runs with fewer lookups take the short-run kernel; default 256 */
+    int32_t chunk;           /* lookups per chunk of a long run; default 256 */
+    int32_t long_run_mode;   /* tbe_long_run_mode */
+    int32_t hist_mode;       /* tbe_hist_mode */
+    /* Optional timing hook: when kernel_events is non-NULL, the library
+     * records kernel_events[2i] before and kernel_events[2i+1] after its
+     * i-th kernel launch of the call on `stream` (up to n_kernel_events
+     * pairs), and writes the kernel's name pointer to kernel_names[i] when
+     * kernel_names is non-NULL.  *kernel_events_used (host) receives the
+     * number of pairs recorded. */
+    cudaEvent_t *kernel_events;
+    const char **kernel_names;
+    int32_t n_kernel_events;
+    int32_t *kernel_events_used;
+} tbe_config;
+
+/* The tables: all T tables stored back to back in one [rows_total, D] array. */
+typedef struct tbe_tables {
+    void *weights;                      /* device, [rows_total, D] of dtype, 16-byte aligned */
+    const int64_t *table_offset;        /* device, [T+1]: table t owns rows [off[t], off[t+1]) */
+    const int64_t *table_offset_host;   /* host copy of the same [T+1] values */
+    int32_t T;
+    int32_t D;
+    int32_t dtype;                      /* tbe_dtype */
+} tbe_tables;
+
+/* One batch in KeyedJagged CSR form. */
+typedef struct tbe_batch {
+    const int32_t *indices;             /* device, [N]; row index within its table */
+    const int32_t *offsets;             /* device, [T*B+1]; offsets[0] = 0, offsets[T*B] = N */
+    int64_t N;                          /* number of lookups, 0 <= N < 2^30 */
+    int64_t B;                          /* bags per table */
+    const float *per_sample_weights;    /* device, [N] or NULL (unweighted) */
+    const uint8_t *weighted_tables;     /* device, [T] or NULL: nonzero = table uses the weights;
+                                           NULL with weights given = every table weighted */
+} tbe_batch;
+
+/*
+ * Batch-inversion metadata (FBTriton TBE redesign, "Forward state reuse and
+ * preprocessing" and "transpose_embedding_input"): produced by tbe_forward
+ * (when given a meta) or tbe_preprocess, consumed by the backward.  Bind it to
+ * a caller device buffer with tbe_meta_bind; the fields are device pointers
+ * into that buffer plus the problem it was bound for, and are read-only to
+ * the caller.  After a generic-path forward/preprocess, on the device:
+ *   sorted_keys[0..N)  linearised keys table_offset[t]+idx in ascending order,
+ *                      out-of-range lookups last with key = rows_total
+ *   sorted_vals[0..N)  payload in the same (stable) order: the bag index b
+ *                      within its table when the batch is unweighted, else
+ *                      the lookup position p (bag_of[p] then gives t*B+b)
+ *   unique_keys[0..U), seg_off[0..U]  run r = positions [seg_off[r], seg_off[r+1])
+ *   counters[0] = U (unique rows), counters[1] = N' (in-range lookups),
+ *   counters[2] = long runs, counters[3] = chunks of long runs
+ * After a histogram-path forward/preprocess: hist[(t*B+b)*64 + e] holds the
+ * FP16 count of lookups of row e in bag (t,b).
+ */
+typedef struct tbe_meta {
+    int64_t bound_N, bound_B;
+    int32_t bound_T, path;              /* path: 1 = generic, 2 = histogram */
+    int32_t payload_is_pos, key_bits;
+    int64_t rows_total;
+    uint32_t *sorted_keys, *sorted_vals;
+    uint32_t *keys_a, *vals_a, *keys_b, *vals_b;
+    int32_t *bag_of;
+    uint32_t *unique_keys;
+    int32_t *seg_off;
+    int32_t *counters;
+    int32_t *long_run;                  /* [max_long] run id of long run l */
+    int32_t *long_chunk_base;           /* [max_long] first chunk slot of long run l */
+    int32_t *chunk_owner;               /* [max_chunks] long run of chunk slot c */
+    int32_t *arrive;                    /* [max_long] arrival counters of the fused long-run path */
+    uint16_t *hist;
+    size_t bytes;
+} tbe_meta;
+
+/* Fill *cfg with the defaults (SL threshold 256, chunk 256, AUTO modes, no events). */
+void tbe_config_default(tbe_config *cfg);
+
+/*
+ * Device memory the caller must provide for this problem: the meta buffer
+ * (bound with tbe_meta_bind) and the scratch workspace passed to every call.
+ * One workspace may serve forward, preprocess and backward in turn on one
+ * stream.  Returns TBE_OK or an argument error for an unsupported problem.
+ */
+tbe_status tbe_query_sizes(const tbe_tables *tables, const tbe_batch *batch,
+                           const tbe_config *cfg, size_t *meta_bytes, size_t *workspace_bytes);
+
+/* Carve `meta` out of device_buf (>= meta_bytes, 256-byte aligned).  Host only. */
+tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes,
+                         const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);
+
+/*
+ * Forward pooled lookup with fused bounds check (decision checklist item 5):
+ * writes out[B, T*D] (device, float32; every element written, empty bags give
+ * 0).  Out-of-range indices contribute nothing and are counted into
+ * dev_status[0].  Accumulation is FP32 for FP16/BF16 tables and FP64 for FP32
+ * tables (decision checklist item 1).
+ * When `meta` is non-NULL the batch inversion also runs here ("Forward state
+ * reuse and preprocessing": sort and RLE moved into forward) and the
+ * backward reuses it; on the histogram path the forward saves its counts.
+ */
+tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *out,
+                       tbe_meta *meta, void *workspace, size_t workspace_bytes,
+                       int32_t *dev_status, const tbe_config *cfg, cudaStream_t stream);
+
+/*
+ * Batch inversion alone (the pages' default placement, at the start of the
+ * backward): linearise (t,idx) to int32 keys (decision checklist item 6),
+ * stable radix sort, run-length encode, route runs by segment length.  On
+ * the histogram path: build the per-bag counts.  Fills `meta`.
+ */
+tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_meta *meta,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          const tbe_config *cfg, cudaStream_t stream);
+
+/*
+ * Backward with the fused exact rowwise Adagrad update ("Backward kernels";
+ * TorchEasyRec analysis section 4, fused optimizer).  grad_out is the
+ * gradient of `out` (device, float32 [B, T*D]).  Updates tables->weights and
+ * momentum (device, float32 [rows_total]) in place, once per touched row;
+ * rows no in-range lookup touches are not written.  Runs with SL < 256 take
+ * the short-run kernel; longer runs are reduced in 256-lookup chunks (two
+ * kernels or one fused launch, cfg->long_run_mode).  Weighted tables scale
+ * each gradient row by its per-sample weight before accumulation.
+ * `batch` must be the one `meta` was filled from.
+ */
+tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batch *batch,
+                                        float *momentum, const float *grad_out,
+                                        const tbe_meta *meta, float lr, float eps,
+                                        void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_status, const tbe_config *cfg,
+                                        cudaStream_t stream);
+
+/* Which path tbe_forward will take for this problem: 1 generic, 2 histogram. */
+int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);
+
+/* Static string naming a status code. */
+const char *tbe_status_string(tbe_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t tbe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TBE_GB300_TBE_H */

@@ -1,0 +1,422 @@
+// Backward: per-unique-row gradient reduction with one fused exact rowwise
+// Adagrad update per touched row.
+//
+// FBTriton TBE redesign (accesspath.com), "Backward kernels: three paths by
+// segment length":
+//   short_run      (SL < 256): one owner reduces the whole run, applies the
+//                  optimizer and stores with plain stores (no atomics);
+//   grad_accum + apply (SL >= 256): runs are cut into 256-lookup chunks,
+//                  partial sums go to a workspace, a second kernel applies;
+//   fused          (SL >= 256): same chunks, a device-scope fence lets the
+//                  last-arriving chunk apply the update in the same launch;
+//   weighted tables scale each gradient row by its per-sample weight first.
+// Decision checklist item 1: FP32 accumulation for FP16/BF16 weights, FP64
+// for FP32 weights.  TorchEasyRec analysis (39.107.221.112 article 1724244),
+// section 4: the optimizer update is fused into the backward (one read and
+// one write of each touched row).
+//
+// Design: the owner of a run or chunk is one warp.  Gradient rows are float32
+// [B, T*D]; a row is read as float4 vectors by LPR lanes (NV each), 32/LPR rows
+// per step and U steps in flight.  Partials of chunk slot c live at
+// partials[c*D ...] in the accumulator type.  The long-run sum always adds
+// the chunk partials in chunk order c = 0..k-1, so the two-kernel and the
+// fused modes give bit-identical weights and momentum.  The fused mode needs
+// no waiting: each chunk stores its partial, fences, and bumps the run's
+// arrival counter; only the warp that sees k-1 reads the partials (through
+// L2) and applies, then re-arms the counter.
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+struct BwdParams {
+    void *W;
+    float *mom;
+    const float *G;
+    const int64_t *table_offset;
+    const uint32_t *vals;
+    const int32_t *bag_of;
+    const float *psw;
+    const uint8_t *weighted;
+    const uint32_t *unique_keys;
+    const int32_t *seg_off;
+    const int32_t *counters;
+    const int32_t *long_run;
+    const int32_t *long_chunk_base;
+    const int32_t *chunk_owner;
+    void *partials;
+    int32_t *arrive;
+    int64_t B;
+    int T;
+    int D;
+    float lr;
+    float eps;
+    int sl_threshold;
+    int chunk;
+    int payload_pos;
+};
+
+__device__ __forceinline__ void acc4(double (&a)[4], const float4 x, float w) {
+    a[0] = fma((double)w, (double)x.x, a[0]);
+    a[1] = fma((double)w, (double)x.y, a[1]);
+    a[2] = fma((double)w, (double)x.z, a[2]);
+    a[3] = fma((double)w, (double)x.w, a[3]);
+}
+__device__ __forceinline__ void acc4(float (&a)[4], const float4 x, float w) {
+    a[0] = fmaf(w, x.x, a[0]);
+    a[1] = fmaf(w, x.y, a[1]);
+    a[2] = fmaf(w, x.z, a[2]);
+    a[3] = fmaf(w, x.w, a[3]);
+}
+
+__device__ __forceinline__ void ld4(const float *p, float (&w)[4]) {
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+}
+__device__ __forceinline__ void st4(float *p, const float (&w)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void ld4(const __half *p, float (&w)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+}
+__device__ __forceinline__ void st4(__half *p, const float (&w)[4]) {
+    __half2 a = __halves2half2(__float2half_rn(w[0]), __float2half_rn(w[1]));
+    __half2 b = __halves2half2(__float2half_rn(w[2]), __float2half_rn(w[3]));
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&a);
+    v.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = v;
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16 *p, float (&w)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+}
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float (&w)[4]) {
+    __nv_bfloat162 a = __halves2bfloat162(__float2bfloat16_rn(w[0]), __float2bfloat16_rn(w[1]));
+    __nv_bfloat162 b = __halves2bfloat162(__float2bfloat16_rn(w[2]), __float2bfloat16_rn(w[3]));
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&a);
+    v.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = v;
+}
+
+// partial storage in the accumulator type
+__device__ __forceinline__ void st_part(double *p, const double (&a)[4]) {
+    reinterpret_cast<double2 *>(p)[0] = make_double2(a[0], a[1]);
+    reinterpret_cast<double2 *>(p)[1] = make_double2(a[2], a[3]);
+}
+__device__ __forceinline__ void st_part(float *p, const float (&a)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
+}
+template <bool L2ONLY>
+__device__ __forceinline__ void add_part(double (&a)[4], const double *p) {
+    const double2 x = L2ONLY ? __ldcg(reinterpret_cast<const double2 *>(p))
+                             : __ldg(reinterpret_cast<const double2 *>(p));
+    const double2 y = L2ONLY ? __ldcg(reinterpret_cast<const double2 *>(p) + 1)
+                             : __ldg(reinterpret_cast<const double2 *>(p) + 1);
+    a[0] += x.x; a[1] += x.y; a[2] += y.x; a[3] += y.y;
+}
+template <bool L2ONLY>
+__device__ __forceinline__ void add_part(float (&a)[4], const float *p) {
+    const float4 x = L2ONLY ? __ldcg(reinterpret_cast<const float4 *>(p))
+                            : __ldg(reinterpret_cast<const float4 *>(p));
+    a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+}
+
+// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) into acc (per lane:
+// elements li*4 + q*LPR*4 .. +4), then combine the 32/LPR sub-groups.
+template <typename ACC, int LPR, int NV, int U>
+__device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &p, int t, bool wt,
+                                            int32_t s, int32_t e, int lane, int sub, int li) {
+    constexpr int RPI = 32 / LPR;
+    const float *Gt = p.G + (int64_t)t * p.D + li * 4;
+    const int64_t rowstride = (int64_t)p.T * p.D;
+    const int64_t tB = (int64_t)t * p.B;
+#pragma unroll
+    for (int q = 0; q < NV; ++q)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+    for (int32_t base = s; base < e; base += 32) {
+        const int n = min(32, e - base);
+        int b = 0;
+        float w = 1.f;
+        if (lane < n) {
+            const uint32_t v = __ldg(p.vals + base + lane);
+            if (p.payload_pos) {
+                b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
+                if (wt) w = __ldg(p.psw + v);
+            } else {
+                b = (int)v;
+            }
+            // only malformed (overlapping) offsets can give a bag outside the
+            // run's table; such a lookup contributes nothing
+            if (b < 0 || (int64_t)b >= p.B) {
+                b = 0;
+                w = 0.f;
+            }
+        }
+        for (int j = 0; j < n; j += RPI * U) {
+            float4 x[U][NV];
+            float wv[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = j + u * RPI + sub;
+                const int src = k & 31;
+                const int bk = __shfl_sync(FULL, b, src);
+                wv[u] = __shfl_sync(FULL, w, src);
+                ok[u] = k < n;
+                if (ok[u]) {
+                    const float *r = Gt + (int64_t)bk * rowstride;
+#pragma unroll
+                    for (int q = 0; q < NV; ++q)
+                        x[u][q] = __ldg(reinterpret_cast<const float4 *>(r + q * LPR * 4));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (ok[u])
+#pragma unroll
+                    for (int q = 0; q < NV; ++q) acc4(acc[q], x[u][q], wv[u]);
+        }
+    }
+#pragma unroll
+    for (int sh = LPR; sh < 32; sh <<= 1)
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
+}
+
+// Exact rowwise Adagrad on row `row` from the reduced gradient in acc:
+//   m += mean_d(g^2);  w -= lr * g / (sqrt(m) + eps)
+// Only lanes of sub-group 0 hold meaningful values; every lane takes part in
+// the shuffles.
+template <typename WT, typename ACC, int LPR, int NV>
+__device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const BwdParams &p,
+                                              int64_t row, int lane, int sub, int li) {
+    float gf[NV][4];
+    ACC ss = ACC(0);
+#pragma unroll
+    for (int q = 0; q < NV; ++q)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            gf[q][x] = (float)acc[q][x];
+            ss += (ACC)gf[q][x] * (ACC)gf[q][x];
+        }
+#pragma unroll
+    for (int sh = 1; sh < LPR; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
+    if (sub != 0) return;
+    const float m_old = p.mom[row];
+    const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
+    const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+    WT *wr = reinterpret_cast<WT *>(p.W) + row * p.D + li * 4;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        float w[4];
+        ld4(wr + q * LPR * 4, w);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) w[x] = __fsub_rn(w[x], __fdiv_rn(__fmul_rn(p.lr, gf[q][x]), den));
+        st4(wr + q * LPR * 4, w);
+    }
+    if (lane == 0) p.mom[row] = m_new;
+}
+
+template <typename WT, int LPR, int NV, int U>
+__global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
+    using ACC = typename WTraits<WT>::acc;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int U_runs = p.counters[C_NUM_UNIQUE];
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < U_runs; r += nwarps) {
+        const int32_t s = __ldg(p.seg_off + r), e = __ldg(p.seg_off + r + 1);
+        if (e - s >= p.sl_threshold) continue;
+        const int64_t key = __ldg(p.unique_keys + r);
+        const int t = table_of_key(p.table_offset, p.T, key);
+        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
+        ACC acc[NV][4];
+        gather_rows<ACC, LPR, NV, U>(acc, p, t, wt, s, e, lane, sub, li);
+        adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
+    }
+}
+
+template <typename WT, int LPR, int NV, int U, bool FUSED>
+__global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
+    using ACC = typename WTraits<WT>::acc;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nchunks = p.counters[C_NUM_CHUNKS];
+    for (int ci = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; ci < nchunks; ci += nwarps) {
+        const int l = __ldg(p.chunk_owner + ci);
+        const int r = __ldg(p.long_run + l);
+        const int cb = __ldg(p.long_chunk_base + l);
+        const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
+        const int32_t s = rs + (ci - cb) * p.chunk;
+        const int32_t e = min(s + p.chunk, re);
+        const int64_t key = __ldg(p.unique_keys + r);
+        const int t = table_of_key(p.table_offset, p.T, key);
+        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
+        ACC acc[NV][4];
+        gather_rows<ACC, LPR, NV, U>(acc, p, t, wt, s, e, lane, sub, li);
+        ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
+        if (sub == 0)
+#pragma unroll
+            for (int q = 0; q < NV; ++q) st_part(part + q * LPR * 4, acc[q]);
+        if constexpr (FUSED) {
+            const int nch = (re - rs + p.chunk - 1) / p.chunk;
+            __threadfence();
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atomicAdd(p.arrive + l, 1);
+            old = __shfl_sync(FULL, old, 0);
+            if (old == nch - 1) {
+                __threadfence();
+#pragma unroll
+                for (int q = 0; q < NV; ++q)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+                if (sub == 0)
+                    for (int c = 0; c < nch; ++c) {
+                        const ACC *pp = reinterpret_cast<const ACC *>(p.partials) +
+                                        (int64_t)(cb + c) * p.D + li * 4;
+#pragma unroll
+                        for (int q = 0; q < NV; ++q) add_part<true>(acc[q], pp + q * LPR * 4);
+                    }
+                adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
+                if (lane == 0) p.arrive[l] = 0;
+            }
+        }
+    }
+}
+
+template <typename WT, int LPR, int NV>
+__global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
+    using ACC = typename WTraits<WT>::acc;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nlong = p.counters[C_NUM_LONG];
+    for (int l = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; l < nlong; l += nwarps) {
+        const int r = __ldg(p.long_run + l);
+        const int cb = __ldg(p.long_chunk_base + l);
+        const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
+        const int nch = (re - rs + p.chunk - 1) / p.chunk;
+        const int64_t key = __ldg(p.unique_keys + r);
+        ACC acc[NV][4];
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+        if (sub == 0)
+            for (int c = 0; c < nch; ++c) {
+                const ACC *pp =
+                    reinterpret_cast<const ACC *>(p.partials) + (int64_t)(cb + c) * p.D + li * 4;
+#pragma unroll
+                for (int q = 0; q < NV; ++q) add_part<false>(acc[q], pp + q * LPR * 4);
+            }
+        adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
+    }
+}
+
+// ---------------------------------------------------------------------------
+
+size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype) {
+    const size_t acc = dtype == TBE_F32 ? 8 : 4;
+    return (size_t)max_chunks * (size_t)D * acc;
+}
+
+template <typename K>
+static int persistent_grid(K kernel, int num_sms) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+    if (per_sm < 1) per_sm = 1;
+    return num_sms * per_sm;
+}
+
+template <typename WT, int LPR, int NV>
+static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
+    constexpr int RPI = 32 / LPR;
+    constexpr int U0 = RPI >= 8 ? 1 : (8 / RPI);
+    constexpr int U = (U0 * NV > 8) ? (8 / NV > 0 ? 8 / NV : 1) : U0;
+    if (long_mode == TBE_LONG_TWO_KERNEL) {
+        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, U, false>;
+        L.before("tbe_bwd_grad_accum");
+        kc<<<persistent_grid(kc, L.num_sms), 256, 0, L.stream>>>(p);
+        L.after();
+    } else {
+        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, U, true>;
+        L.before("tbe_bwd_fused_long");
+        kc<<<persistent_grid(kc, L.num_sms), 256, 0, L.stream>>>(p);
+        L.after();
+    }
+    auto ks = tbe_bwd_short_kernel<WT, LPR, NV, U>;
+    L.before("tbe_bwd_short_run");
+    ks<<<persistent_grid(ks, L.num_sms), 256, 0, L.stream>>>(p);
+    L.after();
+    if (long_mode == TBE_LONG_TWO_KERNEL) {
+        auto ka = tbe_bwd_apply_kernel<WT, LPR, NV>;
+        L.before("tbe_bwd_apply");
+        ka<<<persistent_grid(ka, L.num_sms), 256, 0, L.stream>>>(p);
+        L.after();
+    }
+}
+
+template <typename WT>
+static bool bwd_dispatch(Launch &L, const BwdParams &p, RowPlan rp, int long_mode) {
+    switch (rp.lpr * 10 + rp.nv) {
+    case 11: bwd_launch<WT, 1, 1>(L, p, long_mode); return true;
+    case 21: bwd_launch<WT, 2, 1>(L, p, long_mode); return true;
+    case 41: bwd_launch<WT, 4, 1>(L, p, long_mode); return true;
+    case 81: bwd_launch<WT, 8, 1>(L, p, long_mode); return true;
+    case 161: bwd_launch<WT, 16, 1>(L, p, long_mode); return true;
+    case 321: bwd_launch<WT, 32, 1>(L, p, long_mode); return true;
+    case 322: bwd_launch<WT, 32, 2>(L, p, long_mode); return true;
+    case 323: bwd_launch<WT, 32, 3>(L, p, long_mode); return true;
+    case 324: bwd_launch<WT, 32, 4>(L, p, long_mode); return true;
+    default: return false;
+    }
+}
+
+tbe_status launch_backward(Launch &L, const BwdArgs &a) {
+    const tbe_meta *m = a.meta;
+    BwdParams p;
+    p.W = a.tab->weights;
+    p.mom = a.momentum;
+    p.G = a.grad_out;
+    p.table_offset = a.tab->table_offset;
+    p.vals = m->sorted_vals;
+    p.bag_of = m->bag_of;
+    p.psw = a.bt->per_sample_weights;
+    p.weighted = a.bt->weighted_tables;
+    p.unique_keys = m->unique_keys;
+    p.seg_off = m->seg_off;
+    p.counters = m->counters;
+    p.long_run = m->long_run;
+    p.long_chunk_base = m->long_chunk_base;
+    p.chunk_owner = m->chunk_owner;
+    p.partials = a.partials;
+    p.arrive = a.arrive;
+    p.B = a.bt->B;
+    p.T = a.tab->T;
+    p.D = a.tab->D;
+    p.lr = a.lr;
+    p.eps = a.eps;
+    p.sl_threshold = a.sl_threshold;
+    p.chunk = a.chunk;
+    p.payload_pos = m->payload_is_pos;
+    if (a.bt->N == 0) return TBE_OK;
+    const RowPlan rp = row_plan(a.tab->D, 4);
+    bool ok = false;
+    switch (a.tab->dtype) {
+    case TBE_F32: ok = bwd_dispatch<float>(L, p, rp, a.long_mode); break;
+    case TBE_F16: ok = bwd_dispatch<__half>(L, p, rp, a.long_mode); break;
+    case TBE_BF16: ok = bwd_dispatch<__nv_bfloat16>(L, p, rp, a.long_mode); break;
+    default: return TBE_ERR_UNSUPPORTED_DTYPE;
+    }
+    return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
+}
+
+}  // namespace tbe

@@ -1,0 +1,305 @@
+// Stable LSD radix sort of (key, payload) pairs: the sort step of the batch
+// inversion (FBTriton TBE redesign, accesspath.com, "transpose_embedding_input";
+// decision checklist item 6: int32 keys halve the sort-key width).  Only the
+// significant key bits are sorted: ceil(key_bits / 8) passes of 8 bits.
+//
+// Design (onesweep: one read and one write of the pairs per pass, digit
+// prefixes across tiles by decoupled look-back):
+//  1. one histogram kernel counts every pass's digits at once and zeroes the
+//     look-back state; a 256-thread kernel per pass turns counts into bucket
+//     starts;
+//  2. per pass, CTAs take tiles in ticket order (an atomic counter, so a
+//     CTA only ever waits for tiles that CTAs already running hold).  A tile
+//     of 4096 pairs is ranked stably inside the CTA (per-warp match_any
+//     ranking in input order, then warp prefixes), each digit's tile count is
+//     published, and thread d looks back over earlier tiles for digit d's
+//     running prefix.  The tile is reordered by digit in shared memory and
+//     written out, so each digit's run of pairs lands contiguously.
+//  The look-back status word packs a 2-bit state and a 30-bit count (so
+//  N < 2^30).  Every wait is bounded: after MAX_SPINS polls the CTA sets
+//  TBE_FLAG_SORT_TIMEOUT in the status word and carries on (the sort output
+//  is then invalid, which the flag reports).
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+constexpr int RADIX_BITS = 8;
+constexpr int RADIX = 256;
+constexpr int SORT_THREADS = 256;
+constexpr int SORT_WARPS = SORT_THREADS / 32;
+constexpr int SORT_IPT = 16;
+constexpr int SORT_TILE = SORT_THREADS * SORT_IPT;   // 4096
+constexpr uint32_t ST_AGG = 1u << 30;
+constexpr uint32_t ST_INC = 2u << 30;
+constexpr uint32_t ST_MASK = (1u << 30) - 1;
+constexpr int MAX_PASSES = 4;
+constexpr long long MAX_SPINS = 1ll << 24;
+
+static int num_passes(int key_bits) { return (key_bits + RADIX_BITS - 1) / RADIX_BITS; }
+
+struct SortWs {
+    uint32_t *hist;        // [MAX_PASSES][256] digit counts, then bucket starts
+    uint32_t *tickets;     // [MAX_PASSES] tile tickets
+    uint32_t *status;      // [MAX_PASSES][ntiles][256] look-back words
+    int64_t ntiles;
+};
+
+static SortWs carve(void *ws, int64_t N) {
+    SortWs s;
+    s.ntiles = (N + SORT_TILE - 1) / SORT_TILE;
+    char *p = (char *)ws;
+    s.hist = (uint32_t *)p;
+    p += MAX_PASSES * RADIX * 4;
+    s.tickets = (uint32_t *)p;
+    p += 256;
+    s.status = (uint32_t *)p;
+    return s;
+}
+
+size_t sort_workspace_bytes(int64_t N, int key_bits) {
+    const int64_t ntiles = (N + SORT_TILE - 1) / SORT_TILE;
+    (void)key_bits;
+    return MAX_PASSES * RADIX * 4 + 256 + (size_t)MAX_PASSES * ntiles * RADIX * 4 + 256;
+}
+
+__global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t *__restrict__ keys, int64_t N,
+                                                         int passes, uint32_t *hist,
+                                                         uint32_t *zero, int64_t zero_words) {
+    __shared__ uint32_t sh[MAX_PASSES * RADIX];
+    for (int i = threadIdx.x; i < MAX_PASSES * RADIX; i += blockDim.x) sh[i] = 0;
+    __syncthreads();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t N4 = N / 4;
+    for (int64_t i = tid; i < N4; i += stride) {
+        const uint4 k4 = __ldg(reinterpret_cast<const uint4 *>(keys) + i);
+        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            for (int ps = 0; ps < passes; ++ps)
+                atomicAdd(&sh[ps * RADIX + ((kk[e] >> (ps * RADIX_BITS)) & (RADIX - 1))], 1u);
+    }
+    for (int64_t i = N4 * 4 + tid; i < N; i += stride) {
+        const uint32_t k = __ldg(keys + i);
+        for (int ps = 0; ps < passes; ++ps)
+            atomicAdd(&sh[ps * RADIX + ((k >> (ps * RADIX_BITS)) & (RADIX - 1))], 1u);
+    }
+    for (int64_t i = tid; i < zero_words; i += stride) zero[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < passes * RADIX; i += blockDim.x)
+        if (sh[i]) atomicAdd(&hist[i], sh[i]);
+}
+
+// Exclusive scan of one pass's 256 digit counts into bucket starts, in place.
+__global__ void __launch_bounds__(256) radix_bucket_kernel(uint32_t *hist) {
+    __shared__ uint32_t s[RADIX];
+    uint32_t *h = hist + blockIdx.x * RADIX;
+    const int d = threadIdx.x;
+    s[d] = h[d];
+    __syncthreads();
+    for (int off = 1; off < RADIX; off <<= 1) {
+        uint32_t v = d >= off ? s[d - off] : 0;
+        __syncthreads();
+        s[d] += v;
+        __syncthreads();
+    }
+    h[d] = s[d] - h[d];
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+struct PassSmem {
+    uint32_t keys[SORT_TILE];
+    uint32_t vals[SORT_TILE];
+    uint32_t warp_cnt[SORT_WARPS][RADIX];   // counts, then exclusive warp prefixes
+    uint32_t count[RADIX];
+    uint32_t local_off[RADIX];
+    uint32_t global_base[RADIX];
+    uint32_t warp_tot[SORT_WARPS];
+    uint32_t tile;
+};
+
+__global__ void __launch_bounds__(SORT_THREADS, 2)
+radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
+                      uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t N,
+                      int shift, const uint32_t *__restrict__ bucket, uint32_t *status,
+                      uint32_t *ticket, int32_t *err) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    PassSmem &S = *reinterpret_cast<PassSmem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) S.tile = atomicAdd(ticket, 1u);
+    for (int i = tid; i < SORT_WARPS * RADIX; i += SORT_THREADS) (&S.warp_cnt[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t tile = S.tile;
+    const int64_t tile_base = tile * SORT_TILE;
+
+    // warp-striped load: item i of lane l in warp w sits at tile position
+    // w*32*IPT + i*32 + l, so (i, lane) order within a warp is input order
+    uint32_t k[SORT_IPT], v[SORT_IPT], rank[SORT_IPT];
+#pragma unroll
+    for (int i = 0; i < SORT_IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+        const bool ok = pos < N;
+        k[i] = ok ? __ldg(keys_in + pos) : 0xffffffffu;
+        v[i] = ok ? __ldg(vals_in + pos) : 0u;
+    }
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int i = 0; i < SORT_IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+        const uint32_t d = pos < N ? ((k[i] >> shift) & (RADIX - 1)) : RADIX;   // RADIX = padding
+        const unsigned peers = __match_any_sync(FULL, d);
+        const int leader = __ffs(peers) - 1;
+        uint32_t base = 0;
+        if (lane == leader && d < RADIX) {
+            base = S.warp_cnt[warp][d];
+            S.warp_cnt[warp][d] = base + __popc(peers);
+        }
+        base = __shfl_sync(FULL, base, leader);
+        rank[i] = base + __popc(peers & lt);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // per digit: tile count and exclusive prefix over warps
+    {
+        const int d = tid;   // SORT_THREADS == RADIX
+        uint32_t sum = 0;
+#pragma unroll
+        for (int w = 0; w < SORT_WARPS; ++w) {
+            const uint32_t c = S.warp_cnt[w][d];
+            S.warp_cnt[w][d] = sum;
+            sum += c;
+        }
+        S.count[d] = sum;
+
+        // publish this tile's count, then look back for the running prefix
+        uint32_t excl = 0;
+        uint32_t *st = status + tile * RADIX + d;
+        if (tile == 0) {
+            st_relaxed_u32(st, ST_INC | sum);
+        } else {
+            st_relaxed_u32(st, ST_AGG | sum);
+            int64_t j = tile - 1;
+            long long spins = 0;
+            while (true) {
+                const uint32_t s = ld_relaxed_u32(status + j * RADIX + d);
+                const uint32_t f = s & ~ST_MASK;
+                if (f == 0) {
+                    if (++spins > MAX_SPINS) {
+                        atomicOr(err, TBE_FLAG_SORT_TIMEOUT);
+                        break;
+                    }
+                    __nanosleep(64);
+                    continue;
+                }
+                excl += s & ST_MASK;
+                if (f == ST_INC || j == 0) break;
+                --j;
+            }
+            st_relaxed_u32(st, ST_INC | (excl + sum));
+        }
+        S.global_base[d] = __ldg(bucket + d) + excl;
+
+        // exclusive scan of the tile's digit counts (warp scans + warp totals)
+        uint32_t x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) S.warp_tot[warp] = x;
+        __syncthreads();
+        uint32_t wp = 0;
+        for (int w = 0; w < warp; ++w) wp += S.warp_tot[w];
+        S.local_off[d] = wp + x - sum;
+    }
+    __syncthreads();
+
+    // reorder the tile by digit in shared memory
+#pragma unroll
+    for (int i = 0; i < SORT_IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+        if (pos < N) {
+            const uint32_t d = (k[i] >> shift) & (RADIX - 1);
+            const uint32_t lp = S.local_off[d] + S.warp_cnt[warp][d] + rank[i];
+            S.keys[lp] = k[i];
+            S.vals[lp] = v[i];
+        }
+    }
+    __syncthreads();
+
+    const int64_t rem = N - tile_base;
+    const int n = rem < SORT_TILE ? (int)rem : SORT_TILE;
+    for (int j = tid; j < n; j += SORT_THREADS) {
+        const uint32_t key = S.keys[j];
+        const uint32_t d = (key >> shift) & (RADIX - 1);
+        const uint32_t gp = S.global_base[d] + (j - S.local_off[d]);
+        if ((int64_t)gp < N) {   // always true unless a look-back gave up (flagged)
+            keys_out[gp] = key;
+            vals_out[gp] = S.vals[j];
+        }
+    }
+}
+
+__global__ void fill_u32_kernel(uint32_t *p, int64_t n, uint32_t v) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = v;
+}
+
+tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *keys_b,
+                       uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
+                       bool *in_b) {
+    const int passes = num_passes(key_bits);
+    *in_b = (passes & 1) != 0;
+    if (N == 0 || passes == 0) {
+        *in_b = false;
+        return TBE_OK;
+    }
+    if (passes > MAX_PASSES) return TBE_ERR_KEY_RANGE;
+    SortWs s = carve(ws, N);
+    const int64_t zero_words = (int64_t)passes * s.ntiles * RADIX;
+
+    L.before("tbe_sort_zero");
+    fill_u32_kernel<<<1, 256, 0, L.stream>>>(s.hist, MAX_PASSES * RADIX + 64, 0u);
+    L.after();
+
+    int hist_grid = (int)((N / 4 + 255) / 256);
+    if (hist_grid > L.num_sms * 4) hist_grid = L.num_sms * 4;
+    if (hist_grid < 1) hist_grid = 1;
+    L.before("tbe_sort_histogram");
+    radix_hist_kernel<<<hist_grid, 256, 0, L.stream>>>(keys_a, N, passes, s.hist, s.status,
+                                                       zero_words);
+    L.after();
+    L.before("tbe_sort_buckets");
+    radix_bucket_kernel<<<passes, RADIX, 0, L.stream>>>(s.hist);
+    L.after();
+
+    const size_t smem = sizeof(PassSmem);
+    static_assert(sizeof(PassSmem) < 227 * 1024, "pass shared memory");
+    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    const uint32_t *ki = keys_a, *vi = vals_a;
+    uint32_t *ko = keys_b, *vo = vals_b;
+    for (int ps = 0; ps < passes; ++ps) {
+        L.before("tbe_sort_onesweep");
+        radix_onesweep_kernel<<<(unsigned)s.ntiles, SORT_THREADS, smem, L.stream>>>(
+            ki, vi, ko, vo, N, ps * RADIX_BITS, s.hist + ps * RADIX,
+            s.status + (int64_t)ps * s.ntiles * RADIX, s.tickets + ps, status + 1);
+        L.after();
+        const uint32_t *tk = ko, *tv = vo;
+        ko = const_cast<uint32_t *>(ki);
+        vo = const_cast<uint32_t *>(vi);
+        ki = tk;
+        vi = tv;
+    }
+    return TBE_OK;
+}
+
+}  // namespace tbe

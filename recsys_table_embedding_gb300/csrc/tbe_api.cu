@@ -1,0 +1,371 @@
+// Host side of the C ABI declared in tbe.h: argument checks, buffer sizing,
+// metadata binding and the order of kernel launches for each entry point.
+// Everything here runs on the host and only enqueues work on the caller's
+// stream; no device memory is allocated and no host synchronisation happens.
+#include <string.h>
+
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+void Launch::before(const char *name) {
+    if (cfg == nullptr || cfg->kernel_events == nullptr || used >= cfg->n_kernel_events) return;
+    cudaEventRecord(cfg->kernel_events[2 * used], stream);
+    if (cfg->kernel_names != nullptr) cfg->kernel_names[used] = name;
+}
+
+void Launch::after() {
+    if (cudaPeekAtLastError() != cudaSuccess) failed = true;
+    if (cfg == nullptr || cfg->kernel_events == nullptr || used >= cfg->n_kernel_events) return;
+    cudaEventRecord(cfg->kernel_events[2 * used + 1], stream);
+    ++used;
+    if (cfg->kernel_events_used != nullptr) *cfg->kernel_events_used = used;
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static int bits_for(int64_t v) {   // bits needed to represent v >= 0
+    int b = 0;
+    while (b < 63 && (v >> b) != 0) ++b;
+    return b;
+}
+
+struct Problem {
+    int64_t N, B, NB, rows_total, max_rows;
+    int T, D, dtype;
+    int key_bits;
+    int path;           // 1 generic, 2 histogram
+    int payload_pos;
+    int64_t max_long, max_chunks;
+    int sl_threshold, chunk, long_mode;
+};
+
+static tbe_config defaults(const tbe_config *cfg) {
+    tbe_config c;
+    tbe_config_default(&c);
+    if (cfg != nullptr) {
+        c = *cfg;
+        if (c.sl_threshold <= 0) c.sl_threshold = 256;
+        if (c.chunk <= 0) c.chunk = 256;
+    }
+    return c;
+}
+
+static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, const tbe_config *cfg,
+                                Problem *pr) {
+    if (tab == nullptr || bt == nullptr) return TBE_ERR_NULL_POINTER;
+    if (tab->weights == nullptr || tab->table_offset == nullptr || tab->table_offset_host == nullptr)
+        return TBE_ERR_NULL_POINTER;
+    if (tab->T < 1 || tab->D < 1) return TBE_ERR_INVALID_ARGUMENT;
+    if (tab->dtype != TBE_F32 && tab->dtype != TBE_F16 && tab->dtype != TBE_BF16)
+        return TBE_ERR_UNSUPPORTED_DTYPE;
+    if (bt->N < 0 || bt->N >= (int64_t(1) << 30) || bt->B < 0) return TBE_ERR_INVALID_ARGUMENT;
+    if ((int64_t)tab->T * bt->B >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
+    if (bt->offsets == nullptr) return TBE_ERR_NULL_POINTER;
+    if (bt->N > 0 && bt->indices == nullptr) return TBE_ERR_NULL_POINTER;
+    if (!aligned(tab->weights, 16) || !aligned(tab->table_offset, 8) || !aligned(bt->offsets, 4) ||
+        !aligned(bt->indices, 4) || !aligned(bt->per_sample_weights, 4))
+        return TBE_ERR_MISALIGNED;
+    const int64_t *to = tab->table_offset_host;
+    if (to[0] != 0) return TBE_ERR_INVALID_ARGUMENT;
+    int64_t max_rows = 0;
+    for (int t = 0; t < tab->T; ++t) {
+        if (to[t + 1] < to[t]) return TBE_ERR_INVALID_ARGUMENT;
+        if (to[t + 1] - to[t] > max_rows) max_rows = to[t + 1] - to[t];
+    }
+    const int64_t rows_total = to[tab->T];
+    // int32 linearised keys (decision checklist item 6); rows_total itself
+    // is the sentinel key of out-of-range lookups, so it must fit too
+    if (rows_total >= (int64_t(1) << 31) - 1) return TBE_ERR_KEY_RANGE;
+    const int esz = tab->dtype == TBE_F32 ? 4 : 2;
+    if (!row_plan(tab->D, esz).ok || !row_plan(tab->D, 4).ok) return TBE_ERR_UNSUPPORTED_DIM;
+    tbe_config c = defaults(cfg);
+    if (c.long_run_mode < 0 || c.long_run_mode > 2 || c.hist_mode < 0 || c.hist_mode > 2)
+        return TBE_ERR_INVALID_ARGUMENT;
+    pr->N = bt->N;
+    pr->B = bt->B;
+    pr->NB = (int64_t)tab->T * bt->B;
+    pr->T = tab->T;
+    pr->D = tab->D;
+    pr->dtype = tab->dtype;
+    pr->rows_total = rows_total;
+    pr->max_rows = max_rows;
+    pr->key_bits = bits_for(rows_total);
+    pr->payload_pos = bt->per_sample_weights != nullptr ? 1 : 0;
+    pr->sl_threshold = c.sl_threshold;
+    pr->chunk = c.chunk;
+    pr->long_mode = c.long_run_mode == TBE_LONG_TWO_KERNEL ? TBE_LONG_TWO_KERNEL : TBE_LONG_FUSED;
+    pr->max_long = bt->N / c.sl_threshold + 1;
+    pr->max_chunks = bt->N / c.chunk + pr->max_long + 1;
+    pr->path = 1;
+    if (c.hist_mode != TBE_HIST_OFF && hist_shape_ok(tab, bt, max_rows)) {
+        const bool dense_enough = bt->N >= 64 * pr->NB;   // L >= 64 on average
+        if (c.hist_mode == TBE_HIST_FORCE || dense_enough) pr->path = 2;
+    } else if (c.hist_mode == TBE_HIST_FORCE) {
+        return TBE_ERR_HISTOGRAM_SHAPE;
+    }
+    return TBE_OK;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Meta layout (each array 256-byte aligned).
+struct MetaLayout {
+    size_t keys_a, vals_a, keys_b, vals_b, bag_of, unique_keys, seg_off, counters, long_run,
+        long_chunk_base, arrive, chunk_owner, hist, total;
+};
+
+static MetaLayout meta_layout(const Problem &pr) {
+    MetaLayout m;
+    memset(&m, 0, sizeof(m));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    const size_t N = (size_t)pr.N;
+    if (pr.path == 1) {
+        m.keys_a = take(N * 4 + 16);
+        m.vals_a = take(N * 4 + 16);
+        m.keys_b = take(N * 4 + 16);
+        m.vals_b = take(N * 4 + 16);
+        m.bag_of = pr.payload_pos ? take(N * 4 + 16) : (size_t)-1;
+        m.unique_keys = take(N * 4 + 16);
+        m.seg_off = take((N + 1) * 4 + 16);
+        m.counters = take(C_COUNT * 4);
+        m.long_run = take((size_t)pr.max_long * 4);
+        m.long_chunk_base = take((size_t)pr.max_long * 4);
+        m.arrive = take((size_t)pr.max_long * 4);
+        m.chunk_owner = take((size_t)pr.max_chunks * 4);
+        m.hist = (size_t)-1;
+    } else {
+        m.keys_a = m.vals_a = m.keys_b = m.vals_b = m.bag_of = m.unique_keys = m.seg_off =
+            m.long_run = m.long_chunk_base = m.arrive = m.chunk_owner = (size_t)-1;
+        m.counters = take(C_COUNT * 4);
+        m.hist = take((size_t)pr.NB * 64 * 2);
+    }
+    m.total = off;
+    return m;
+}
+
+static size_t workspace_size(const tbe_tables *tab, const tbe_batch *bt, const Problem &pr) {
+    size_t ws = 256;
+    if (pr.path == 1) {
+        size_t pre = sort_workspace_bytes(pr.N, pr.key_bits);
+        const size_t rle = rle_workspace_bytes(pr.N);
+        if (rle > pre) pre = rle;
+        const size_t bwd = bwd_partials_bytes(pr.max_chunks, pr.D, pr.dtype);
+        ws = pre > bwd ? pre : bwd;
+    } else {
+        ws = hist_workspace_bytes(tab, bt);
+    }
+    return align_up(ws + 256, 256);
+}
+
+static tbe_status check_meta(const tbe_meta *meta, const Problem &pr) {
+    if (meta->bound_N != pr.N || meta->bound_B != pr.B || meta->bound_T != pr.T ||
+        meta->path != pr.path || meta->payload_is_pos != pr.payload_pos ||
+        meta->rows_total != pr.rows_total)
+        return TBE_ERR_META;
+    return TBE_OK;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+static tbe_status finish(const Launch &L, tbe_status st) {
+    if (st != TBE_OK) return st;
+    return L.failed ? TBE_ERR_CUDA : TBE_OK;
+}
+
+// linearize (unless the forward already did) + sort + RLE/route, generic path
+static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
+                                tbe_meta *meta, const Problem &pr, void *ws, int32_t *status) {
+    bool in_b = false;
+    tbe_status st = launch_sort(L, meta->keys_a, meta->vals_a, meta->keys_b, meta->vals_b, pr.N,
+                                pr.key_bits, ws, status, &in_b);
+    if (st != TBE_OK) return st;
+    meta->sorted_keys = in_b ? meta->keys_b : meta->keys_a;
+    meta->sorted_vals = in_b ? meta->vals_b : meta->vals_a;
+    return launch_rle(L, meta->sorted_keys, pr.N, (uint32_t)pr.rows_total, meta->unique_keys,
+                      meta->seg_off, meta->counters, meta->long_run, meta->long_chunk_base,
+                      meta->chunk_owner, meta->arrive, pr.sl_threshold, pr.chunk, ws);
+}
+
+}  // namespace tbe
+
+using namespace tbe;
+
+extern "C" {
+
+void tbe_config_default(tbe_config *cfg) {
+    if (cfg == nullptr) return;
+    memset(cfg, 0, sizeof(*cfg));
+    cfg->sl_threshold = 256;
+    cfg->chunk = 256;
+    cfg->long_run_mode = TBE_LONG_AUTO;
+    cfg->hist_mode = TBE_HIST_AUTO;
+}
+
+tbe_status tbe_query_sizes(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg,
+                           size_t *meta_bytes, size_t *workspace_bytes) {
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    if (meta_bytes) *meta_bytes = meta_layout(pr).total;
+    if (workspace_bytes) *workspace_bytes = workspace_size(tables, batch, pr);
+    return TBE_OK;
+}
+
+int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg) {
+    Problem pr;
+    if (check_problem(tables, batch, cfg, &pr) != TBE_OK) return 0;
+    return pr.path;
+}
+
+tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes, const tbe_tables *tables,
+                         const tbe_batch *batch, const tbe_config *cfg) {
+    if (meta == nullptr || device_buf == nullptr) return TBE_ERR_NULL_POINTER;
+    if (!aligned(device_buf, 256)) return TBE_ERR_MISALIGNED;
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    const MetaLayout L = meta_layout(pr);
+    if (bytes < L.total) return TBE_ERR_BUFFER_TOO_SMALL;
+    char *b = (char *)device_buf;
+    auto at = [&](size_t off) -> void * { return off == (size_t)-1 ? nullptr : (void *)(b + off); };
+    memset(meta, 0, sizeof(*meta));
+    meta->bound_N = pr.N;
+    meta->bound_B = pr.B;
+    meta->bound_T = pr.T;
+    meta->path = pr.path;
+    meta->payload_is_pos = pr.payload_pos;
+    meta->key_bits = pr.key_bits;
+    meta->rows_total = pr.rows_total;
+    meta->keys_a = (uint32_t *)at(L.keys_a);
+    meta->vals_a = (uint32_t *)at(L.vals_a);
+    meta->keys_b = (uint32_t *)at(L.keys_b);
+    meta->vals_b = (uint32_t *)at(L.vals_b);
+    meta->sorted_keys = meta->keys_a;
+    meta->sorted_vals = meta->vals_a;
+    meta->bag_of = (int32_t *)at(L.bag_of);
+    meta->unique_keys = (uint32_t *)at(L.unique_keys);
+    meta->seg_off = (int32_t *)at(L.seg_off);
+    meta->counters = (int32_t *)at(L.counters);
+    meta->long_run = (int32_t *)at(L.long_run);
+    meta->long_chunk_base = (int32_t *)at(L.long_chunk_base);
+    meta->chunk_owner = (int32_t *)at(L.chunk_owner);
+    meta->hist = (uint16_t *)at(L.hist);
+    meta->bytes = L.total;
+    meta->arrive = (int32_t *)at(L.arrive);
+    return TBE_OK;
+}
+
+tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *out, tbe_meta *meta,
+                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                       const tbe_config *cfg, cudaStream_t stream) {
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    if (out == nullptr || dev_status == nullptr) return TBE_ERR_NULL_POINTER;
+    if (!aligned(out, 16)) return TBE_ERR_MISALIGNED;
+    if (meta != nullptr) {
+        if ((st = check_meta(meta, pr)) != TBE_OK) return st;
+        if (workspace == nullptr) return TBE_ERR_NULL_POINTER;
+        if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
+    }
+    Launch L{stream, cfg};
+    L.num_sms = sm_count();
+    if (pr.path == 2) {
+        st = launch_hist_forward(L, tables, batch, out, meta ? meta->hist : nullptr, dev_status);
+        return finish(L, st);
+    }
+    st = launch_forward(L, tables, batch, out, meta ? meta->keys_a : nullptr,
+                        meta ? meta->vals_a : nullptr, meta ? meta->bag_of : nullptr,
+                        (uint32_t)pr.rows_total, dev_status);
+    if (st == TBE_OK && meta != nullptr)
+        st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
+    return finish(L, st);
+}
+
+tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_meta *meta,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          const tbe_config *cfg, cudaStream_t stream) {
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    if (meta == nullptr || workspace == nullptr || dev_status == nullptr) return TBE_ERR_NULL_POINTER;
+    if ((st = check_meta(meta, pr)) != TBE_OK) return st;
+    if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
+    Launch L{stream, cfg};
+    L.num_sms = sm_count();
+    if (pr.path == 2) return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status));
+    st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
+                          (uint32_t)pr.rows_total, dev_status);
+    if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
+    return finish(L, st);
+}
+
+tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batch *batch,
+                                        float *momentum, const float *grad_out,
+                                        const tbe_meta *meta, float lr, float eps, void *workspace,
+                                        size_t workspace_bytes, int32_t *dev_status,
+                                        const tbe_config *cfg, cudaStream_t stream) {
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    if (momentum == nullptr || grad_out == nullptr || meta == nullptr || workspace == nullptr ||
+        dev_status == nullptr)
+        return TBE_ERR_NULL_POINTER;
+    if (!aligned(grad_out, 16) || !aligned(momentum, 4) || !aligned(workspace, 256))
+        return TBE_ERR_MISALIGNED;
+    if ((st = check_meta(meta, pr)) != TBE_OK) return st;
+    if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
+    Launch L{stream, cfg};
+    L.num_sms = sm_count();
+    if (pr.path == 2)
+        return finish(L, launch_hist_backward(L, tables, batch, meta->hist, momentum, grad_out, lr,
+                                              eps, workspace, dev_status));
+    BwdArgs a;
+    a.tab = tables;
+    a.bt = batch;
+    a.meta = meta;
+    a.momentum = momentum;
+    a.grad_out = grad_out;
+    a.lr = lr;
+    a.eps = eps;
+    a.partials = workspace;
+    a.arrive = meta->arrive;
+    a.max_chunks = pr.max_chunks;
+    a.max_long = pr.max_long;
+    a.sl_threshold = pr.sl_threshold;
+    a.chunk = pr.chunk;
+    a.long_mode = pr.long_mode;
+    return finish(L, launch_backward(L, a));
+}
+
+const char *tbe_status_string(tbe_status s) {
+    switch (s) {
+    case TBE_OK: return "ok";
+    case TBE_ERR_NULL_POINTER: return "null pointer";
+    case TBE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case TBE_ERR_UNSUPPORTED_DIM: return "unsupported embedding dimension";
+    case TBE_ERR_UNSUPPORTED_DTYPE: return "unsupported weight dtype";
+    case TBE_ERR_MISALIGNED: return "misaligned pointer";
+    case TBE_ERR_KEY_RANGE: return "linearised key range does not fit int32";
+    case TBE_ERR_BUFFER_TOO_SMALL: return "workspace or meta buffer too small";
+    case TBE_ERR_META: return "meta not bound for this problem";
+    case TBE_ERR_HISTOGRAM_SHAPE: return "histogram path does not cover this shape";
+    case TBE_ERR_CUDA: return "CUDA launch failure";
+    }
+    return "unknown status";
+}
+
+int32_t tbe_version(void) { return 100; }
+
+}  // extern "C"

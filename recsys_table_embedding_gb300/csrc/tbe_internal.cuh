@@ -1,0 +1,141 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tbe.h"
+
+namespace tbe {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Indices into meta->counters (device int32).
+enum Counter { C_NUM_UNIQUE = 0, C_N_VALID = 1, C_NUM_LONG = 2, C_NUM_CHUNKS = 3, C_COUNT = 8 };
+
+// Weight element traits: the 16-byte vector of a row, and the accumulator
+// precision (FBTriton TBE redesign, decision checklist item 1: FP32 for
+// FP16/BF16 weights, FP64 for FP32 weights).
+template <typename WT> struct WTraits;
+template <> struct WTraits<float> {
+    using acc = double;
+    static constexpr int VEC = 4;   // elements per 16-byte vector
+};
+template <> struct WTraits<__half> {
+    using acc = float;
+    static constexpr int VEC = 8;
+};
+template <> struct WTraits<__nv_bfloat16> {
+    using acc = float;
+    static constexpr int VEC = 8;
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename WT> __device__ __forceinline__ WT from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Relaxed GPU-scope accesses for flag/status words that carry their own data.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Table of a linearised key: largest t with table_offset[t] <= key (T small).
+__device__ __forceinline__ int table_of_key(const int64_t *table_offset, int T, int64_t key) {
+    int lo = 0, hi = T;   // answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(table_offset + mid) <= key) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch context: the caller's stream, config and optional
+// per-kernel timing events.
+struct Launch {
+    cudaStream_t stream;
+    const tbe_config *cfg;
+    int used = 0;
+    int num_sms = 0;
+    void before(const char *name);
+    void after();
+    bool failed = false;
+};
+
+// Row-vector plan for a D-element row of `bytes_per_elem`: lanes per row
+// (LPR) and 16-byte vectors per lane (NV), with LPR * NV * 16 = row bytes.
+struct RowPlan {
+    int lpr, nv;
+    bool ok;
+};
+RowPlan row_plan(int D, int bytes_per_elem);
+
+// --- forward.cu
+tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
+                          uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+                          int32_t *status);
+tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
+                            uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+                            int32_t *status);
+
+// --- sort.cu: stable LSD radix sort of (key, val) pairs over the low
+// `key_bits` bits; result lands in (keys_a, vals_a) when the number of
+// passes is even, else in (keys_b, vals_b); returns which via *in_b.
+size_t sort_workspace_bytes(int64_t N, int key_bits);
+tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *keys_b,
+                       uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
+                       bool *in_b);
+
+// --- rle.cu: run-length encode sorted keys, route long runs into chunks.
+size_t rle_workspace_bytes(int64_t N);
+tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_t sentinel,
+                      uint32_t *unique_keys, int32_t *seg_off, int32_t *counters,
+                      int32_t *long_run, int32_t *long_chunk_base, int32_t *chunk_owner,
+                      int32_t *arrive, int sl_threshold, int chunk, void *ws);
+
+// --- backward.cu
+struct BwdArgs {
+    const tbe_tables *tab;
+    const tbe_batch *bt;
+    const tbe_meta *meta;
+    float *momentum;
+    const float *grad_out;
+    float lr, eps;
+    void *partials;          // [max_chunks, D] accumulator type
+    int32_t *arrive;         // [max_long]
+    int64_t max_chunks, max_long;
+    int sl_threshold, chunk, long_mode;
+};
+size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype);
+tbe_status launch_backward(Launch &L, const BwdArgs &a);
+
+// --- hist.cu: small-table histogram path on the tensor cores
+bool hist_shape_ok(const tbe_tables *tab, const tbe_batch *bt, int64_t max_rows);
+size_t hist_workspace_bytes(const tbe_tables *tab, const tbe_batch *bt);
+tbe_status launch_hist_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
+                               uint16_t *hist, int32_t *status);
+tbe_status launch_hist_count(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
+                             uint16_t *hist, int32_t *status);
+tbe_status launch_hist_backward(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
+                                const uint16_t *hist, float *momentum, const float *grad_out,
+                                float lr, float eps, void *ws, int32_t *status);
+
+}  // namespace tbe
