@@ -1,0 +1,537 @@
+#!/usr/bin/env python
+"""TBE fwd+bwd (rowwise Adagrad) benchmark on GB300.
+
+One step = tbe_forward (pooled lookup with fused bounds check; on the large
+Zipf workload the batch inversion -- linearise, radix sort, RLE -- runs
+inside it) + tbe_backward_rowwise_adagrad (per-unique-row reduction routed
+by segment length, one exact rowwise Adagrad update per touched row), over
+one synthetic batch already resident in HBM.
+
+Prints one JSON line (rank 0).  Default workload: the large Zipf
+configuration (T=32, E=2M, D=128, bf16, B=131072, L~Poisson(20), ~84M
+lookups, ~3M unique rows, hottest row ~125K lookups).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload large|mid|hist|demo|tiny]
+  python bench.py --impl reference      # the CPU oracle on a bounded sample
+
+With N > 1 (torchrun) every rank runs an independent replica of the whole
+workload (the path has no exchange step on one batch); the value is the
+lookups of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "TBE fwd+bwd (rowwise Adagrad) lookups/s"
+UNIT = "lookups/s"
+PREPROCESS_IN_FORWARD = {"large": True, "mid": False, "demo": False, "tiny": False, "hist": False}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large", choices=sorted(workloads.PRESETS))
+    ap.add_argument("--long-mode", type=int, default=0, help="0 auto, 1 two-kernel, 2 fused")
+    ap.add_argument("--hist-mode", type=int, default=0, help="0 auto, 1 off, 2 force")
+    ap.add_argument("--preprocess", default="config", choices=["config", "forward", "backward"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip e2e, cpu baseline and clocks (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
+    ap.add_argument("--rows", type=int, default=None, help="override E per table (large/mid)")
+    return ap.parse_args()
+
+
+def make_workload(args):
+    kw = {}
+    if args.batch is not None:
+        kw["B"] = args.batch
+    if args.rows is not None and args.workload in ("large", "mid"):
+        kw["E"] = args.rows
+    return workloads.PRESETS[args.workload](**kw)
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(x: float, device, world: int) -> float:
+    """Max of a per-rank float over all ranks (the slowest replica's time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if re.match(r"^[0-9.]+$", r[1])]
+        mx = [float(r[2]) for r in rows if re.match(r"^[0-9.]+$", r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "recsys_table_embedding_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, or None
+    when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != src_hash():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------- bytes
+
+def run_stats(wl, tbe):
+    """Realised batch statistics from the device metadata (generic path)."""
+    import torch
+    from recsys_table_embedding_gb300 import meta_view
+    st = {"N": wl.N, "NB": wl.NB}
+    if tbe.path != 1:
+        return st
+    U, nv, nlong, nchunks = tbe.counters()
+    seg = meta_view(tbe.meta, "seg_off", U + 1, torch.int32).cpu().numpy().astype(np.int64)
+    rl = np.diff(seg)
+    long = rl >= 256
+    st.update(U=U, n_valid=nv, num_long=nlong, num_chunks=nchunks, max_run=int(rl.max()) if U else 0,
+              N_long=int(rl[long].sum()), N_short=int(rl[~long].sum()), U_short=int((~long).sum()))
+    return st
+
+
+def step_bytes(wl, st, pif: bool):
+    """Algorithmic bytes of one step: what the method moves (no re-reads)."""
+    N, NB, D = wl.N, wl.NB, wl.D
+    sw = workloads.DTYPE_BYTES[wl.dtype]
+    nw = 0
+    if wl.per_sample_weights is not None:
+        wt = wl.weighted_tables if wl.weighted_tables is not None else np.ones(wl.T, np.uint8)
+        per_t = np.diff(wl.offsets[::wl.B].astype(np.int64))
+        nw = int(per_t[wt.astype(bool)].sum())
+    if st.get("U") is None:   # histogram path
+        E = 64
+        fwd = 4 * N + 4 * (NB + 1) + NB * D * 4 + NB * E * 2 + int(wl.rows_total) * D * sw
+        bwd = NB * D * 4 + NB * E * 2 + 2 * int(wl.rows_total) * D * sw + 8 * int(wl.rows_total)
+        return {"forward": fwd, "preprocess": 0, "backward": bwd, "total": fwd + bwd}
+    U = st["U"]
+    fwd = 4 * N + 4 * (NB + 1) + 4 * nw + N * D * sw + NB * D * 4
+    pre = 8 * N + 16 * N + 4 * N + 12 * U
+    bwd = 4 * N + 8 * U + 4 * nw + N * D * 4 + 2 * U * D * sw + 8 * U
+    return {"forward": fwd, "preprocess": pre, "backward": bwd, "total": fwd + pre + bwd}
+
+
+def kernel_bytes(name: str, wl, st, pif: bool):
+    """Algorithmic bytes of one launch of the named kernel, or None."""
+    N, NB, D = wl.N, wl.NB, wl.D
+    sw = workloads.DTYPE_BYTES[wl.dtype]
+    if name == "tbe_fwd_gather":
+        return 4 * N + 4 * (NB + 1) + N * D * sw + NB * D * 4 + (8 * N if pif else 0)
+    if name == "tbe_bwd_fused_long" or name == "tbe_bwd_grad_accum":
+        nl = st.get("num_long", 0)
+        b = 4 * st.get("N_long", 0) + st.get("N_long", 0) * D * 4
+        if name == "tbe_bwd_fused_long":
+            b += nl * (2 * D * sw + 8 + 8)
+        return b
+    if name == "tbe_bwd_short_run":
+        us = st.get("U_short", 0)
+        return 4 * st.get("N_short", 0) + st.get("N_short", 0) * D * 4 + us * (2 * D * sw + 8 + 8)
+    if name == "tbe_sort_onesweep":
+        return 16 * N
+    if name == "tbe_hist_fwd_umma":
+        return 4 * N + 4 * (NB + 1) + NB * D * 4 + NB * 64 * 2
+    if name == "tbe_hist_bwd_umma":
+        return NB * D * 4 + NB * 64 * 2
+    return None
+
+
+# ----------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from recsys_table_embedding_gb300 import TBE, Batch, Tables, config, tbe as T
+
+XX
+    cfg = config(long_run_mode=args.long_mode, hist_mode=args.hist_mode)
+
+    W = wl.weights(device=str(dev))
+    tables = Tables(W, wl.table_offset)
+    idx_h = torch.from_numpy(wl.indices)
+    off_h = torch.from_numpy(wl.offsets)
+    G_h = torch.from_numpy(wl.grad_out())
+    psw_h = torch.from_numpy(wl.per_sample_weights) if wl.per_sample_weights is not None else None
+    wt = torch.from_numpy(wl.weighted_tables).to(dev) if wl.weighted_tables is not None else None
+    idx, off, G = idx_h.to(dev), off_h.to(dev), G_h.to(dev)
+    psw = psw_h.to(dev) if psw_h is not None else None
+    batch = Batch(idx, off, wl.B, psw, wt)
+    mom = torch.zeros(wl.rows_total, dtype=torch.float32, device=dev)
+    out = torch.empty((wl.B, wl.T * wl.D), dtype=torch.float32, device=dev)
+    tbe = TBE(tables, batch, cfg, preprocess_in_forward=pif)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(b=batch, o=out, g=G):
+        tbe.forward(b, o)
+        tbe.backward(b, mom, g, wl.lr, wl.eps)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = run_stats(wl, tbe)
+    status = tbe.status.cpu().numpy()
+
+    # per-kernel CUDA events recorded by the library on this stream
+    max_pairs = 64
+    per_call = []
+    for _ in range(2 * args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_pairs)]
+        for e in evs:
+            e.record(stream)     # creates the CUDA event so its handle exists
+        handles = (ctypes.c_void_p * (2 * max_pairs))(*[e.cuda_event for e in evs])
+        names = (ctypes.c_char_p * max_pairs)()
+        used = ctypes.c_int32(0)
+        per_call.append((evs, handles, names, used))
+    torch.cuda.synchronize(dev)
+
+    def arm(i):
+        evs, handles, names, used = per_call[i]
+        cfg.kernel_events = ctypes.cast(handles, ctypes.c_void_p)
+        cfg.kernel_names = ctypes.cast(names, ctypes.c_void_p)
+        cfg.n_kernel_events = max_pairs
+        cfg.kernel_events_used = ctypes.cast(ctypes.pointer(used), ctypes.c_void_p)
+
+    clocks = ClockSampler(local) if not args.quick else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        arm(2 * k)
+        tbe.forward(batch, out)
+        arm(2 * k + 1)
+        tbe.backward(batch, mom, G, wl.lr, wl.eps)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    cfg.kernel_events = None
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    ms_total = t0.elapsed_time(t1)
+
+    # per-kernel durations
+    kern = {}
+    launches = 0
+    for evs, handles, names, used in per_call:
+        launches += used.value
+        for i in range(used.value):
+            nm = names[i].decode()
+            dt = evs[2 * i].elapsed_time(evs[2 * i + 1])
+            d = kern.setdefault(nm, [0, 0.0])
+            d[0] += 1
+            d[1] += dt
+
+    ms_total = reduce_max(ms_total, dev, world)
+    ms_step = ms_total / args.steps
+    value = wl.N * world * args.steps / (ms_total / 1e3)
+
+    # e2e: host pinned inputs -> device, step, result -> host, every step
+    e2e = None
+    if not args.no_e2e and not args.quick:
+        e2e = run_e2e(args, wl, tables, tbe, cfg, idx_h, off_h, G_h, psw_h, wt, mom, dev, world)
+
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_src = "measured" if peaks else "fallback"
+    sb = step_bytes(wl, st, pif)
+    roof = None
+    if kern:
+        dom = max(kern, key=lambda n: kern[n][1])
+        cnt, tot = kern[dom]
+        avg_s = tot / cnt / 1e3
+        kb = kernel_bytes(dom, wl, st, pif)
+        if kb is not None:
+            ach = kb / avg_s / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                    "traffic": ncu_traffic(dom, args.workload), "bytes_per_launch": kb,
+                    "avg_launch_ms": round(avg_s * 1e3, 4), "peak_source": peak_src}
+    step_ach = sb["total"] / (ms_step / 1e3) / 1e9
+    kernels = {n: {"launches": c, "avg_ms": round(t / c, 4), "share": round(t / sum(v[1] for v in kern.values()), 4)}
+               for n, (c, t) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+
+    res = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and not args.quick and world == 1:
+            cpu = cpu_baseline(args.workload)
+        res = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name + ": " + wl.desc,
+                       "weights": wl.dtype, "accumulate": "f64" if wl.dtype == "f32" else "f32",
+                       "preprocess_in_forward": pif, "path": "histogram" if tbe.path == 2 else "generic",
+                       "long_run_mode": args.long_mode, "lookups": wl.N, "bags": wl.NB,
+                       "unique_rows": st.get("U"), "max_run": st.get("max_run"),
+                       "long_runs": st.get("num_long"), "chunks": st.get("num_chunks"),
+                       "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}",
+                       "status_words": [int(x) for x in status[:2]]},
+            "roofline": roof,
+            "step_roofline": {"bytes": sb["total"], "achieved": round(step_ach, 1), "peak": hbm_peak,
+                              "unit": "GB/s", "frac": round(step_ach / hbm_peak, 4),
+                              "frac_of_8tbs_nominal": round(step_ach / 8000.0, 4),
+                              "bytes_split": sb},
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res
+
+
+def run_e2e(args, wl, tables, tbe, cfg, idx_h, off_h, G_h, psw_h, wt, mom, dev, world):
+    """Same step through the public API from pinned host memory: per step the
+    batch (indices, offsets, weights) and the upstream gradient go host->device
+    and the pooled output comes back device->host.  The gradient upload and the
+    output download run on a copy stream, overlapped with the compute."""
+    import torch
+    from recsys_table_embedding_gb300 import Batch
+    idx_p, off_p, G_p = idx_h.pin_memory(), off_h.pin_memory(), G_h.pin_memory()
+    psw_p = psw_h.pin_memory() if psw_h is not None else None
+    out_p = torch.empty((wl.B, wl.T * wl.D), dtype=torch.float32).pin_memory()
+    idx_d, off_d = torch.empty_like(idx_h, device=dev), torch.empty_like(off_h, device=dev)
+    G_d = torch.empty_like(G_h, device=dev)
+    psw_d = torch.empty_like(psw_h, device=dev) if psw_h is not None else None
+    out_d = torch.empty((wl.B, wl.T * wl.D), dtype=torch.float32, device=dev)
+    batch = Batch(idx_d, off_d, wl.B, psw_d, wt)
+    main = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    h2d = idx_h.numel() * 4 + off_h.numel() * 4 + G_h.numel() * 4 + (psw_h.numel() * 4 if psw_h is not None else 0)
+    d2h = out_p.numel() * 4
+
+    def e2e_step():
+        idx_d.copy_(idx_p, non_blocking=True)
+        off_d.copy_(off_p, non_blocking=True)
+        if psw_d is not None:
+            psw_d.copy_(psw_p, non_blocking=True)
+        copy.wait_stream(main)            # previous step's backward is done with G_d
+        with torch.cuda.stream(copy):
+            G_d.copy_(G_p, non_blocking=True)
+        tbe.forward(batch, out_d)
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(main)
+        copy.wait_event(fwd_done)
+        with torch.cuda.stream(copy):
+            out_p.copy_(out_d, non_blocking=True)
+        main.wait_stream(copy)            # G_d uploaded (and out copied) before backward/next step
+        tbe.backward(batch, mom, G_d, wl.lr, wl.eps)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    for _ in range(steps):
+        e2e_step()
+    b.record(main)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(a.elapsed_time(b), dev, world)
+    return {"value": round(wl.N * world * steps / (ms / 1e3), 1), "unit": UNIT,
+            "ms_per_step": round(ms / steps, 4), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------- oracle
+
+def oracle_sample(workload: str, tables: int):
+    """A bounded sample of the workload for the CPU oracle: its first `tables`
+    tables with all their bags (same indices and offsets), fresh weights of
+    the same distribution and an upstream gradient for them."""
+    wl = workloads.PRESETS[workload]()
+    k = min(tables, wl.T)
+    end = int(wl.offsets[k * wl.B])
+    sub = workloads.Workload(
+        name=wl.name, T=k, B=wl.B, D=wl.D, dtype=wl.dtype, table_rows=wl.table_rows[:k].copy(),
+        offsets=wl.offsets[:k * wl.B + 1].copy(), indices=wl.indices[:end].copy(),
+        per_sample_weights=wl.per_sample_weights[:end].copy() if wl.per_sample_weights is not None else None,
+        weighted_tables=wl.weighted_tables[:k].copy() if wl.weighted_tables is not None else None,
+        lr=wl.lr, eps=wl.eps, seed=wl.seed)
+    rng = np.random.default_rng(99)
+    Wf = rng.uniform(-wl.w_init, wl.w_init, size=(sub.rows_total, wl.D)).astype(np.float32)
+    if wl.dtype == "f32":
+        W = Wf
+    else:
+        import torch
+        W = torch.from_numpy(Wf).to(sub.torch_dtype()).view(torch.int16).numpy().view(np.uint16)
+    G = rng.standard_normal((wl.B, k * wl.D), dtype=np.float32)
+    return sub, W, G, wl
+
+
+def oracle_step(sub, W, G):
+    import oracle
+    oracle.forward(sub, W)
+    oracle.backward_adagrad(sub, W, sub.momentum(), G)
+
+
+def cpu_baseline(workload: str):
+    import oracle
+    oracle.build()
+    k = {"large": 4, "mid": 4, "hist": 8, "demo": 16, "tiny": 2}[workload]
+    sub, W, G, _ = oracle_sample(workload, k)
+    t = time.perf_counter()
+    oracle_step(sub, W, G)
+    dt = time.perf_counter() - t
+    return {"value": round(sub.N / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"first {sub.T} tables of the workload with all their bags ({sub.N} lookups): "
+                      f"forward + batch inversion + backward with Adagrad, single-threaded plain C, "
+                      f"double accumulation"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    sub, W, G, wl = oracle_sample(args.workload, 1)
+    for _ in range(args.warmup):
+        oracle_step(sub, W, G)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sub, W, G)
+    dt = time.perf_counter() - t
+    value = sub.N * args.steps / dt
+    pif = PREPROCESS_IN_FORWARD[args.workload]
+    sample = (f"table 0 of the {wl.T}-table workload with all its {wl.B} bags ({sub.N} lookups) per step: "
+              f"forward + batch inversion + backward with Adagrad, single-threaded plain C oracle")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name + ": " + wl.desc, "weights": wl.dtype,
+                      "preprocess_in_forward": pif},
+           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return res
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

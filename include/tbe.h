@@ -99,11 +99,12 @@ typedef struct tbe_config {
     int32_t long_run_mode;   /* tbe_long_run_mode */
     int32_t hist_mode;       /* tbe_hist_mode */
     /* Optional timing hook: when kernel_events is non-NULL, the library
-     * records kernel_events[2i] before and kernel_events[2i+1] after its
-     * i-th kernel launch of the call on `stream` (up to n_kernel_events
-     * pairs), and writes the kernel's name pointer to kernel_names[i] when
-     * kernel_names is non-NULL.  *kernel_events_used (host) receives the
-     * number of pairs recorded. */
+     * records kernel_events[2i] before and kernel_events[2i+1] after each of
+     * its kernel launches on `stream`, for i = *kernel_events_used, +1, ...
+     * up to n_kernel_events pairs, writes the kernel's static name to
+     * kernel_names[i] when kernel_names is non-NULL, and advances
+     * *kernel_events_used (host int, required with kernel_events), so
+     * consecutive calls append. */
     cudaEvent_t *kernel_events;
     const char **kernel_names;
     int32_t n_kernel_events;

@@ -8,6 +8,11 @@
 
 namespace tbe {
 
+Launch::Launch(cudaStream_t s, const tbe_config *c) : stream(s), cfg(c) {
+    // event recording continues after the pairs earlier calls recorded
+    if (cfg != nullptr && cfg->kernel_events_used != nullptr) used = *cfg->kernel_events_used;
+}
+
 void Launch::before(const char *name) {
     if (cfg == nullptr || cfg->kernel_events == nullptr || used >= cfg->n_kernel_events) return;
     cudaEventRecord(cfg->kernel_events[2 * used], stream);
@@ -77,8 +82,6 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     // int32 linearised keys (decision checklist item 6); rows_total itself
     // is the sentinel key of out-of-range lookups, so it must fit too
     if (rows_total >= (int64_t(1) << 31) - 1) return TBE_ERR_KEY_RANGE;
-    const int esz = tab->dtype == TBE_F32 ? 4 : 2;
-    if (!row_plan(tab->D, esz).ok || !row_plan(tab->D, 4).ok) return TBE_ERR_UNSUPPORTED_DIM;
     tbe_config c = defaults(cfg);
     if (c.long_run_mode < 0 || c.long_run_mode > 2 || c.hist_mode < 0 || c.hist_mode > 2)
         return TBE_ERR_INVALID_ARGUMENT;
@@ -104,6 +107,10 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     } else if (c.hist_mode == TBE_HIST_FORCE) {
         return TBE_ERR_HISTOGRAM_SHAPE;
     }
+    // the generic path reads weight rows and gradient rows as 16-byte vectors
+    const int esz = tab->dtype == TBE_F32 ? 4 : 2;
+    if (pr->path == 1 && (!row_plan(tab->D, esz).ok || !row_plan(tab->D, 4).ok))
+        return TBE_ERR_UNSUPPORTED_DIM;
     return TBE_OK;
 }
 
@@ -279,7 +286,7 @@ tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *
         if (workspace == nullptr) return TBE_ERR_NULL_POINTER;
         if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
     }
-    Launch L{stream, cfg};
+    Launch L(stream, cfg);
     L.num_sms = sm_count();
     if (pr.path == 2) {
         st = launch_hist_forward(L, tables, batch, out, meta ? meta->hist : nullptr, dev_status);
@@ -302,7 +309,7 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
     if (meta == nullptr || workspace == nullptr || dev_status == nullptr) return TBE_ERR_NULL_POINTER;
     if ((st = check_meta(meta, pr)) != TBE_OK) return st;
     if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
-    Launch L{stream, cfg};
+    Launch L(stream, cfg);
     L.num_sms = sm_count();
     if (pr.path == 2) return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status));
     st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
@@ -326,7 +333,7 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
         return TBE_ERR_MISALIGNED;
     if ((st = check_meta(meta, pr)) != TBE_OK) return st;
     if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
-    Launch L{stream, cfg};
+    Launch L(stream, cfg);
     L.num_sms = sm_count();
     if (pr.path == 2)
         return finish(L, launch_hist_backward(L, tables, batch, meta->hist, momentum, grad_out, lr,

@@ -75,9 +75,10 @@ struct Launch {
     const tbe_config *cfg;
     int used = 0;
     int num_sms = 0;
+    bool failed = false;
+    Launch(cudaStream_t s, const tbe_config *c);
     void before(const char *name);
     void after();
-    bool failed = false;
 };
 
 // Row-vector plan for a D-element row of `bytes_per_elem`: lanes per row
