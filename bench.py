@@ -242,7 +242,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     from recsys_table_embedding_gb300 import TBE, Batch, Tables, config, tbe as T
 
-XX
+    wl = make_workload(args)
+    pif = PREPROCESS_IN_FORWARD[args.workload] if args.preprocess == "config" else args.preprocess == "forward"
     cfg = config(long_run_mode=args.long_mode, hist_mode=args.hist_mode)
 
     W = wl.weights(device=str(dev))
