@@ -411,33 +411,50 @@ def run_e2e(args, wl, tables, tbe, cfg, idx_h, off_h, G_h, psw_h, wt, mom, dev, 
     h2d = idx_h.numel() * 4 + off_h.numel() * 4 + G_h.numel() * 4 + (psw_h.numel() * 4 if psw_h is not None else 0)
     d2h = out_p.numel() * 4
 
+    ev = {"out_copied": None, "bwd_done": None}
+
     def e2e_step():
+        # the previous step's output download must finish before out_d is rewritten
+        if ev["out_copied"] is not None:
+            main.wait_event(ev["out_copied"])
         idx_d.copy_(idx_p, non_blocking=True)
         off_d.copy_(off_p, non_blocking=True)
         if psw_d is not None:
             psw_d.copy_(psw_p, non_blocking=True)
-        copy.wait_stream(main)            # previous step's backward is done with G_d
+        # gradient upload on the copy stream, once the previous backward is done with G_d
+        if ev["bwd_done"] is not None:
+            copy.wait_event(ev["bwd_done"])
         with torch.cuda.stream(copy):
             G_d.copy_(G_p, non_blocking=True)
+        g_ready = torch.cuda.Event()
+        g_ready.record(copy)
         tbe.forward(batch, out_d)
         fwd_done = torch.cuda.Event()
         fwd_done.record(main)
+        # output download overlaps the backward
         copy.wait_event(fwd_done)
         with torch.cuda.stream(copy):
             out_p.copy_(out_d, non_blocking=True)
-        main.wait_stream(copy)            # G_d uploaded (and out copied) before backward/next step
+        out_copied = torch.cuda.Event()
+        out_copied.record(copy)
+        main.wait_event(g_ready)
         tbe.backward(batch, mom, G_d, wl.lr, wl.eps)
+        bwd_done = torch.cuda.Event()
+        bwd_done.record(main)
+        ev["out_copied"], ev["bwd_done"] = out_copied, bwd_done
 
     steps = max(3, min(args.steps, 10))
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize(dev)
+    ev["out_copied"] = ev["bwd_done"] = None
     if world > 1:
         torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(main)
     for _ in range(steps):
         e2e_step()
+    main.wait_event(ev["out_copied"])
     b.record(main)
     torch.cuda.synchronize(dev)
     ms = reduce_max(a.elapsed_time(b), dev, world)

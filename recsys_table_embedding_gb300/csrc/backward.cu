@@ -113,26 +113,80 @@ __device__ __forceinline__ void st_part(float *p, const float (&a)[4]) {
     *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
 }
 template <bool L2ONLY>
-__device__ __forceinline__ void add_part(double (&a)[4], const double *p) {
+__device__ __forceinline__ void ld_part(double (&a)[4], const double *p) {
     const double2 x = L2ONLY ? __ldcg(reinterpret_cast<const double2 *>(p))
                              : __ldg(reinterpret_cast<const double2 *>(p));
     const double2 y = L2ONLY ? __ldcg(reinterpret_cast<const double2 *>(p) + 1)
                              : __ldg(reinterpret_cast<const double2 *>(p) + 1);
-    a[0] += x.x; a[1] += x.y; a[2] += y.x; a[3] += y.y;
+    a[0] = x.x; a[1] = x.y; a[2] = y.x; a[3] = y.y;
 }
 template <bool L2ONLY>
-__device__ __forceinline__ void add_part(float (&a)[4], const float *p) {
+__device__ __forceinline__ void ld_part(float (&a)[4], const float *p) {
     const float4 x = L2ONLY ? __ldcg(reinterpret_cast<const float4 *>(p))
                             : __ldg(reinterpret_cast<const float4 *>(p));
-    a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+    a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
 }
 
-// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) into acc (per lane:
-// elements li*4 + q*LPR*4 .. +4), then combine the 32/LPR sub-groups.
-template <typename ACC, int LPR, int NV, int U>
+// acc += partials of chunk slots cb .. cb+nch-1, added strictly in chunk
+// order; PB slots are loaded ahead so that many loads are in flight.
+template <bool L2ONLY, typename ACC, int LPR, int NV>
+__device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], const ACC *part, int cb, int nch,
+                                             int D, int li) {
+    constexpr int PB = NV >= 2 ? 2 : 4;
+    for (int c0 = 0; c0 < nch; c0 += PB) {
+        ACC v[PB][NV][4];
+#pragma unroll
+        for (int j = 0; j < PB; ++j)
+            if (c0 + j < nch)
+#pragma unroll
+                for (int q = 0; q < NV; ++q)
+                    ld_part<L2ONLY>(v[j][q], part + (int64_t)(cb + c0 + j) * D + li * 4 + q * LPR * 4);
+#pragma unroll
+        for (int j = 0; j < PB; ++j)
+            if (c0 + j < nch)
+#pragma unroll
+                for (int q = 0; q < NV; ++q)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[q][x] += v[j][q][x];
+    }
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ring depth (steps) of the asynchronous gather for NV vectors per lane.
+template <int NV> struct Ring {
+    static constexpr int S = NV == 1 ? 20 : (NV == 2 ? 10 : 5);
+};
+// shared memory of one warp: the ring [S][NV][32] float4, then the bag and
+// weight of each lookup of the chunk
+template <int NV> __host__ __device__ constexpr int warp_smem_bytes(int chunk) {
+    return Ring<NV>::S * NV * 32 * 16 + chunk * 8;
+}
+
+// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) (at most `chunk`
+// of them) into acc (per lane: elements li*4 + q*LPR*4 .. +4), then combine
+// the 32/LPR sub-groups.  Gradient rows are copied with cp.async into a
+// per-warp ring of S steps (RPI rows per step), so S-1 steps of rows are in
+// flight without holding registers; each lane copies and later reads back
+// only its own 16-byte vectors.
+template <typename ACC, int LPR, int NV>
 __device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &p, int t, bool wt,
-                                            int32_t s, int32_t e, int lane, int sub, int li) {
+                                            int32_t s, int32_t e, int lane, int sub, int li,
+                                            float4 *ring, int *pb, float *pw) {
     constexpr int RPI = 32 / LPR;
+    constexpr int S = Ring<NV>::S;
+    constexpr int DEPTH = S - 1;
     const float *Gt = p.G + (int64_t)t * p.D + li * 4;
     const int64_t rowstride = (int64_t)p.T * p.D;
     const int64_t tB = (int64_t)t * p.B;
@@ -140,48 +194,49 @@ __device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &
     for (int q = 0; q < NV; ++q)
 #pragma unroll
         for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
-    for (int32_t base = s; base < e; base += 32) {
-        const int n = min(32, e - base);
-        int b = 0;
+    const int n = e - s;
+    __syncwarp();   // the previous range's readers are done with pb/pw
+    for (int i = lane; i < n; i += 32) {
+        const uint32_t v = __ldg(p.vals + s + i);
+        int b;
         float w = 1.f;
-        if (lane < n) {
-            const uint32_t v = __ldg(p.vals + base + lane);
-            if (p.payload_pos) {
-                b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
-                if (wt) w = __ldg(p.psw + v);
-            } else {
-                b = (int)v;
-            }
-            // only malformed (overlapping) offsets can give a bag outside the
-            // run's table; such a lookup contributes nothing
-            if (b < 0 || (int64_t)b >= p.B) {
-                b = 0;
-                w = 0.f;
-            }
+        if (p.payload_pos) {
+            b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
+            if (wt) w = __ldg(p.psw + v);
+        } else {
+            b = (int)v;
         }
-        for (int j = 0; j < n; j += RPI * U) {
-            float4 x[U][NV];
-            float wv[U];
-            bool ok[U];
+        // only malformed (overlapping) offsets can give a bag outside the
+        // run's table; such a lookup contributes nothing
+        pb[i] = (b >= 0 && (int64_t)b < p.B) ? b : -1;
+        pw[i] = w;
+    }
+    __syncwarp();
+    const int nsteps = (n + RPI - 1) / RPI;
+    int slot_in = 0, slot_out = 0;
+    for (int k = 0; k < nsteps + DEPTH; ++k) {
+        if (k < nsteps) {
+            const int i = k * RPI + sub;
+            const int b = i < n ? pb[i] : -1;
+            if (b >= 0) {
+                const float *src = Gt + (int64_t)b * rowstride;
+                float4 *dst = ring + slot_in * NV * 32 + lane;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = j + u * RPI + sub;
-                const int src = k & 31;
-                const int bk = __shfl_sync(FULL, b, src);
-                wv[u] = __shfl_sync(FULL, w, src);
-                ok[u] = k < n;
-                if (ok[u]) {
-                    const float *r = Gt + (int64_t)bk * rowstride;
-#pragma unroll
-                    for (int q = 0; q < NV; ++q)
-                        x[u][q] = __ldg(reinterpret_cast<const float4 *>(r + q * LPR * 4));
-                }
+                for (int q = 0; q < NV; ++q) cp_async16(smem_addr(dst + q * 32), src + q * LPR * 4);
             }
+            slot_in = slot_in + 1 == S ? 0 : slot_in + 1;
+        }
+        cp_async_commit();
+        if (k >= DEPTH) {
+            cp_async_wait<DEPTH>();
+            const int i = (k - DEPTH) * RPI + sub;
+            if (i < n && pb[i] >= 0) {
+                const float w = pw[i];
+                const float4 *src = ring + slot_out * NV * 32 + lane;
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (ok[u])
-#pragma unroll
-                    for (int q = 0; q < NV; ++q) acc4(acc[q], x[u][q], wv[u]);
+                for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * 32], w);
+            }
+            slot_out = slot_out + 1 == S ? 0 : slot_out + 1;
         }
     }
 #pragma unroll
@@ -226,30 +281,151 @@ __device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const Bwd
     if (lane == 0) p.mom[row] = m_new;
 }
 
-template <typename WT, int LPR, int NV, int U>
+// Raw weight slices held between the prefetch and the update.
+template <typename WT> struct WRaw;
+template <> struct WRaw<float> { using t = float4; };
+template <> struct WRaw<__half> { using t = uint2; };
+template <> struct WRaw<__nv_bfloat16> { using t = uint2; };
+
+template <typename WT>
+__device__ __forceinline__ typename WRaw<WT>::t ld_wraw(const WT *p) {
+    return *reinterpret_cast<const typename WRaw<WT>::t *>(p);
+}
+__device__ __forceinline__ void unpack_w(const float4 r, float (&w)[4]) {
+    w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+}
+__device__ __forceinline__ void unpack_w(const uint2 r, float (&w)[4], __half) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+}
+__device__ __forceinline__ void unpack_w(const uint2 r, float (&w)[4], __nv_bfloat16) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+}
+template <typename WT>
+__device__ __forceinline__ void unpack(const typename WRaw<WT>::t r, float (&w)[4]) {
+    if constexpr (sizeof(WT) == 4) unpack_w(r, w);
+    else unpack_w(r, w, WT());
+}
+
+// Short runs (SL < sl_threshold): a group of GL lanes owns one run, so a warp
+// works on 32/GL runs at once.  Lane gl of a group holds vectors
+// gl + q*GL (q < NV) of the row (float4 of the gradient, 4 weights).  The
+// weight slice and the momentum are loaded before the gather so their
+// latency overlaps it; U gradient rows of the run are in flight per step.
+template <typename WT, int GL, int NV, int U>
 __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
-    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    constexpr int GPW = 32 / GL;
+    const int lane = threadIdx.x & 31, grp = lane / GL, gl = lane % GL;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int U_runs = p.counters[C_NUM_UNIQUE];
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < U_runs; r += nwarps) {
-        const int32_t s = __ldg(p.seg_off + r), e = __ldg(p.seg_off + r + 1);
-        if (e - s >= p.sl_threshold) continue;
-        const int64_t key = __ldg(p.unique_keys + r);
-        const int t = table_of_key(p.table_offset, p.T, key);
-        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
+    const int64_t TD = (int64_t)p.T * p.D;
+    for (int rb = warp * GPW; rb < U_runs; rb += nwarps * GPW) {
+        const int r = rb + grp;
+        int32_t s = 0, e = 0;
+        int64_t key = 0;
+        if (r < U_runs) {
+            s = __ldg(p.seg_off + r);
+            e = __ldg(p.seg_off + r + 1);
+            key = __ldg(p.unique_keys + r);
+        }
+        const bool mine = r < U_runs && e - s < p.sl_threshold;
         ACC acc[NV][4];
-        gather_rows<ACC, LPR, NV, U>(acc, p, t, wt, s, e, lane, sub, li);
-        adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+        typename WRaw<WT>::t wraw[NV];
+        float m_old = 0.f;
+        WT *wr = reinterpret_cast<WT *>(p.W) + key * p.D;
+        if (mine) {
+#pragma unroll
+            for (int q = 0; q < NV; ++q) wraw[q] = ld_wraw(wr + (gl + q * GL) * 4);
+            m_old = p.mom[key];
+            const int t = table_of_key(p.table_offset, p.T, key);
+            const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
+            const float *Gt = p.G + (int64_t)t * p.D + gl * 4;
+            const int64_t tB = (int64_t)t * p.B;
+            for (int32_t i = s; i < e; i += U) {
+                int bk[U];
+                float wk[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    bk[u] = -1;
+                    wk[u] = 1.f;
+                    if (i + u < e) {
+                        const uint32_t v = __ldg(p.vals + i + u);
+                        int b;
+                        if (p.payload_pos) {
+                            b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
+                            if (wt) wk[u] = __ldg(p.psw + v);
+                        } else {
+                            b = (int)v;
+                        }
+                        // only malformed (overlapping) offsets can give a bag
+                        // outside the run's table; such a lookup adds nothing
+                        bk[u] = (b >= 0 && (int64_t)b < p.B) ? b : -1;
+                    }
+                }
+                float4 x[U][NV];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (bk[u] >= 0)
+#pragma unroll
+                        for (int q = 0; q < NV; ++q)
+                            x[u][q] = __ldg(reinterpret_cast<const float4 *>(
+                                Gt + (int64_t)bk[u] * TD + q * GL * 4));
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (bk[u] >= 0)
+#pragma unroll
+                        for (int q = 0; q < NV; ++q) acc4(acc[q], x[u][q], wk[u]);
+            }
+        }
+        // exact rowwise Adagrad: m += mean_d g^2; w -= lr * g / (sqrt(m) + eps)
+        float gf[NV][4];
+        ACC ss = ACC(0);
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                gf[q][x] = (float)acc[q][x];
+                ss += (ACC)gf[q][x] * (ACC)gf[q][x];
+            }
+#pragma unroll
+        for (int o = 1; o < GL; o <<= 1) ss += __shfl_xor_sync(FULL, ss, o);
+        if (mine) {
+            const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
+            const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                float w[4];
+                unpack<WT>(wraw[q], w);
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    w[x] = __fsub_rn(w[x], __fdiv_rn(__fmul_rn(p.lr, gf[q][x]), den));
+                st4(wr + (gl + q * GL) * 4, w);
+            }
+            if (gl == 0) p.mom[key] = m_new;
+        }
     }
 }
 
-template <typename WT, int LPR, int NV, int U, bool FUSED>
+template <typename WT, int LPR, int NV, bool FUSED>
 __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nchunks = p.counters[C_NUM_CHUNKS];
+    unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * warp_smem_bytes<NV>(p.chunk);
+    float4 *ring = reinterpret_cast<float4 *>(wsm);
+    int *pb = reinterpret_cast<int *>(wsm + Ring<NV>::S * NV * 32 * 16);
+    float *pw = reinterpret_cast<float *>(pb + p.chunk);
     for (int ci = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; ci < nchunks; ci += nwarps) {
         const int l = __ldg(p.chunk_owner + ci);
         const int r = __ldg(p.long_run + l);
@@ -261,7 +437,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
         const int t = table_of_key(p.table_offset, p.T, key);
         const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         ACC acc[NV][4];
-        gather_rows<ACC, LPR, NV, U>(acc, p, t, wt, s, e, lane, sub, li);
+        gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, ring, pb, pw);
         ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
         if (sub == 0)
 #pragma unroll
@@ -280,12 +456,8 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
 #pragma unroll
                     for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
                 if (sub == 0)
-                    for (int c = 0; c < nch; ++c) {
-                        const ACC *pp = reinterpret_cast<const ACC *>(p.partials) +
-                                        (int64_t)(cb + c) * p.D + li * 4;
-#pragma unroll
-                        for (int q = 0; q < NV; ++q) add_part<true>(acc[q], pp + q * LPR * 4);
-                    }
+                    sum_partials<true, ACC, LPR, NV>(acc, reinterpret_cast<const ACC *>(p.partials),
+                                                    cb, nch, p.D, li);
                 adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
                 if (lane == 0) p.arrive[l] = 0;
             }
@@ -311,12 +483,8 @@ __global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
         if (sub == 0)
-            for (int c = 0; c < nch; ++c) {
-                const ACC *pp =
-                    reinterpret_cast<const ACC *>(p.partials) + (int64_t)(cb + c) * p.D + li * 4;
-#pragma unroll
-                for (int q = 0; q < NV; ++q) add_part<false>(acc[q], pp + q * LPR * 4);
-            }
+            sum_partials<false, ACC, LPR, NV>(acc, reinterpret_cast<const ACC *>(p.partials), cb,
+                                              nch, p.D, li);
         adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
     }
 }
@@ -329,30 +497,44 @@ size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype) {
 }
 
 template <typename K>
-static int persistent_grid(K kernel, int num_sms) {
+static int persistent_grid(K kernel, int num_sms, size_t smem = 0) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem);
     if (per_sm < 1) per_sm = 1;
     return num_sms * per_sm;
 }
 
+static constexpr bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+// vectors per lane of the short-run kernel: as many as 4, with a power-of-two group
+static constexpr int short_vectors_per_lane(int V) {
+    return (V % 4 == 0 && pow2(V / 4)) ? 4
+           : (V % 3 == 0 && pow2(V / 3)) ? 3
+           : (V % 2 == 0 && pow2(V / 2)) ? 2 : 1;
+}
+
 template <typename WT, int LPR, int NV>
 static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
-    constexpr int RPI = 32 / LPR;
-    constexpr int U0 = RPI >= 8 ? 1 : (8 / RPI);
-    constexpr int U = (U0 * NV > 8) ? (8 / NV > 0 ? 8 / NV : 1) : U0;
+    const size_t csm = (size_t)8 * warp_smem_bytes<NV>(p.chunk);
     if (long_mode == TBE_LONG_TWO_KERNEL) {
-        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, U, false>;
+        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, false>;
+        cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
         L.before("tbe_bwd_grad_accum");
-        kc<<<persistent_grid(kc, L.num_sms), 256, 0, L.stream>>>(p);
+        kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
         L.after();
     } else {
-        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, U, true>;
+        auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, true>;
+        cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
         L.before("tbe_bwd_fused_long");
-        kc<<<persistent_grid(kc, L.num_sms), 256, 0, L.stream>>>(p);
+        kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
         L.after();
     }
-    auto ks = tbe_bwd_short_kernel<WT, LPR, NV, U>;
+    // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
+    constexpr int V = LPR * NV;                       // float4 vectors per gradient row
+    constexpr int SNV = short_vectors_per_lane(V);
+    constexpr int SGL = V / SNV;
+    static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0, "short-run lane groups");
+    constexpr int SU = SNV >= 3 ? 2 : 4;
+    auto ks = tbe_bwd_short_kernel<WT, SGL, SNV, SU>;
     L.before("tbe_bwd_short_run");
     ks<<<persistent_grid(ks, L.num_sms), 256, 0, L.stream>>>(p);
     L.after();

@@ -25,9 +25,9 @@ namespace tbe {
 
 constexpr int RADIX_BITS = 8;
 constexpr int RADIX = 256;
-constexpr int SORT_THREADS = 256;
+constexpr int SORT_THREADS = 512;
 constexpr int SORT_WARPS = SORT_THREADS / 32;
-constexpr int SORT_IPT = 16;
+constexpr int SORT_IPT = 8;
 constexpr int SORT_TILE = SORT_THREADS * SORT_IPT;   // 4096
 constexpr uint32_t ST_AGG = 1u << 30;
 constexpr uint32_t ST_INC = 2u << 30;
@@ -119,7 +119,7 @@ struct PassSmem {
     uint32_t count[RADIX];
     uint32_t local_off[RADIX];
     uint32_t global_base[RADIX];
-    uint32_t warp_tot[SORT_WARPS];
+    uint32_t warp_tot[RADIX / 32];
     uint32_t tile;
 };
 
@@ -166,10 +166,11 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     }
     __syncthreads();
 
-    // per digit: tile count and exclusive prefix over warps
-    {
-        const int d = tid;   // SORT_THREADS == RADIX
-        uint32_t sum = 0;
+    // per digit (threads 0..255): tile count and exclusive prefix over warps,
+    // then the look-back for the digit's prefix over earlier tiles
+    const int d = tid;
+    uint32_t sum = 0, x = 0;
+    if (d < RADIX) {
 #pragma unroll
         for (int w = 0; w < SORT_WARPS; ++w) {
             const uint32_t c = S.warp_cnt[w][d];
@@ -178,7 +179,6 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
         }
         S.count[d] = sum;
 
-        // publish this tile's count, then look back for the running prefix
         uint32_t excl = 0;
         uint32_t *st = status + tile * RADIX + d;
         if (tile == 0) {
@@ -207,14 +207,16 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
         S.global_base[d] = __ldg(bucket + d) + excl;
 
         // exclusive scan of the tile's digit counts (warp scans + warp totals)
-        uint32_t x = sum;
+        x = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(FULL, x, o);
             if (lane >= o) x += y;
         }
         if (lane == 31) S.warp_tot[warp] = x;
-        __syncthreads();
+    }
+    __syncthreads();
+    if (d < RADIX) {
         uint32_t wp = 0;
         for (int w = 0; w < warp; ++w) wp += S.warp_tot[w];
         S.local_off[d] = wp + x - sum;
