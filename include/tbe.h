@@ -74,6 +74,7 @@ typedef enum tbe_dtype { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
 #define TBE_FLAG_SORT_TIMEOUT  0x4  /* radix-sort look-back gave up waiting: sort output invalid */
 #define TBE_FLAG_HIST_COUNT    0x8  /* a histogram count exceeded 2048 (not exact in FP16) */
 #define TBE_FLAG_MMA_TIMEOUT   0x10 /* a tensor-core completion wait gave up: output invalid */
+#define TBE_FLAG_COPY_TIMEOUT  0x20 /* a bulk-copy completion wait gave up: output invalid */
 #define TBE_STATUS_WORDS 4
 
 /* Where runs with SL >= sl_threshold are reduced (FBTriton TBE redesign,
@@ -95,7 +96,7 @@ typedef enum tbe_hist_mode {
 
 typedef struct tbe_config {
     int32_t sl_threshold;    /* runs with fewer lookups take the short-run kernel; default 256 */
-    int32_t chunk;           /* lookups per chunk of a long run; default 256 */
+    int32_t chunk;           /* lookups per chunk of a long run, 32..1024; default 256 */
     int32_t long_run_mode;   /* tbe_long_run_mode */
     int32_t hist_mode;       /* tbe_hist_mode */
     /* Optional timing hook: when kernel_events is non-NULL, the library

@@ -45,6 +45,7 @@ struct BwdParams {
     const int32_t *chunk_owner;
     void *partials;
     int32_t *arrive;
+    int32_t *status;
     int64_t B;
     int T;
     int D;
@@ -154,40 +155,82 @@ __device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], const ACC *part,
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// ---- bulk-copy gather ------------------------------------------------------
+// One lane issues a cp.async.bulk (the TMA engine's non-tensor copy) per
+// gradient row into a per-warp ring of STAGES stages of 4 KB; each stage's
+// mbarrier completes when all its bytes have landed.  Lanes then read their
+// own 16-byte vectors of each row from shared memory.
+
+constexpr int STAGES = 3;
+constexpr int STAGE_BYTES = 4096;
+constexpr long long BAR_WAIT_LIMIT = 1ll << 26;
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
+__device__ __forceinline__ void bar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
 }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
-// Ring depth (steps) of the asynchronous gather for NV vectors per lane.
-template <int NV> struct Ring {
-    static constexpr int S = NV == 1 ? 20 : (NV == 2 ? 10 : 5);
+// shared memory of one warp: STAGES x STAGE_BYTES ring, STAGES mbarriers,
+// then the element offset and weight of each lookup of the range
+__host__ __device__ constexpr int warp_smem_bytes(int chunk) {
+    return (STAGES * STAGE_BYTES + 64 + chunk * 8 + 127) / 128 * 128;
+}
+
+struct WarpRing {
+    unsigned char *ring;
+    uint32_t bar0;        // shared address of the first mbarrier
+    uint32_t *off;        // element offset of each lookup's gradient row from G_t
+    float *w;
+    uint32_t phase;       // bit s = parity of stage s's next completion
 };
-// shared memory of one warp: the ring [S][NV][32] float4, then the bag and
-// weight of each lookup of the chunk
-template <int NV> __host__ __device__ constexpr int warp_smem_bytes(int chunk) {
-    return Ring<NV>::S * NV * 32 * 16 + chunk * 8;
+
+__device__ __forceinline__ WarpRing warp_ring(unsigned char *wsm, int chunk, int lane) {
+    WarpRing r;
+    r.ring = wsm;
+    r.bar0 = smem_addr(wsm + STAGES * STAGE_BYTES);
+    r.off = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);
+    r.w = reinterpret_cast<float *>(r.off + chunk);
+    r.phase = 0;
+    if (lane == 0)
+        for (int i = 0; i < STAGES; ++i) bar_init(r.bar0 + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    return r;
 }
 
-// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) (at most `chunk`
-// of them) into acc (per lane: elements li*4 + q*LPR*4 .. +4), then combine
-// the 32/LPR sub-groups.  Gradient rows are copied with cp.async into a
-// per-warp ring of S steps (RPI rows per step), so S-1 steps of rows are in
-// flight without holding registers; each lane copies and later reads back
-// only its own 16-byte vectors.
+// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) (at most `chunk`)
+// into acc (per lane: elements li*4 + q*LPR*4 .. +4), then combine the 32/LPR
+// sub-groups.  Returns false if a copy wait gave up (bounded).
 template <typename ACC, int LPR, int NV>
-__device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &p, int t, bool wt,
+__device__ __forceinline__ bool gather_rows(ACC (&acc)[NV][4], const BwdParams &p, int t, bool wt,
                                             int32_t s, int32_t e, int lane, int sub, int li,
-                                            float4 *ring, int *pb, float *pw) {
+                                            WarpRing &rg) {
     constexpr int RPI = 32 / LPR;
-    constexpr int S = Ring<NV>::S;
-    constexpr int DEPTH = S - 1;
-    const float *Gt = p.G + (int64_t)t * p.D + li * 4;
+    const uint32_t row_bytes = (uint32_t)p.D * 4;
+    const int R = STAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
+    const float *Gt = p.G + (int64_t)t * p.D;
     const int64_t rowstride = (int64_t)p.T * p.D;
     const int64_t tB = (int64_t)t * p.B;
 #pragma unroll
@@ -195,7 +238,7 @@ __device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &
 #pragma unroll
         for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
     const int n = e - s;
-    __syncwarp();   // the previous range's readers are done with pb/pw
+    __syncwarp();   // the previous range's readers are done with off/w
     for (int i = lane; i < n; i += 32) {
         const uint32_t v = __ldg(p.vals + s + i);
         int b;
@@ -207,37 +250,46 @@ __device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &
             b = (int)v;
         }
         // only malformed (overlapping) offsets can give a bag outside the
-        // run's table; such a lookup contributes nothing
-        pb[i] = (b >= 0 && (int64_t)b < p.B) ? b : -1;
-        pw[i] = w;
+        // run's table: such a lookup copies row 0 with weight 0
+        const bool ok = b >= 0 && (int64_t)b < p.B;
+        rg.off[i] = ok ? (uint32_t)((int64_t)b * rowstride) : 0u;
+        rg.w[i] = ok ? w : 0.f;
     }
     __syncwarp();
-    const int nsteps = (n + RPI - 1) / RPI;
-    int slot_in = 0, slot_out = 0;
-    for (int k = 0; k < nsteps + DEPTH; ++k) {
-        if (k < nsteps) {
-            const int i = k * RPI + sub;
-            const int b = i < n ? pb[i] : -1;
-            if (b >= 0) {
-                const float *src = Gt + (int64_t)b * rowstride;
-                float4 *dst = ring + slot_in * NV * 32 + lane;
-#pragma unroll
-                for (int q = 0; q < NV; ++q) cp_async16(smem_addr(dst + q * 32), src + q * LPR * 4);
+    const int nst = (n + R - 1) / R;
+    auto produce = [&](int k) {
+        const int st = k % STAGES;
+        const int rows = min(R, n - k * R);
+        const uint32_t bar = rg.bar0 + 8 * st;
+        if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
+        __syncwarp();
+        const uint32_t dst0 = smem_addr(rg.ring + st * STAGE_BYTES);
+        for (int j = lane; j < rows; j += 32)
+            bulk_g2s(dst0 + j * row_bytes, Gt + rg.off[k * R + j], row_bytes, bar);
+    };
+    for (int k = 0; k < nst && k < STAGES; ++k) produce(k);
+    bool ok = true;
+    for (int k = 0; k < nst; ++k) {
+        const int st = k % STAGES;
+        const uint32_t bar = rg.bar0 + 8 * st;
+        const uint32_t par = (rg.phase >> st) & 1u;
+        long long spins = 0;
+        while (!bar_try_wait(bar, par))
+            if (++spins > BAR_WAIT_LIMIT) {
+                ok = false;
+                break;
             }
-            slot_in = slot_in + 1 == S ? 0 : slot_in + 1;
-        }
-        cp_async_commit();
-        if (k >= DEPTH) {
-            cp_async_wait<DEPTH>();
-            const int i = (k - DEPTH) * RPI + sub;
-            if (i < n && pb[i] >= 0) {
-                const float w = pw[i];
-                const float4 *src = ring + slot_out * NV * 32 + lane;
+        rg.phase ^= 1u << st;
+        const int rows = min(R, n - k * R);
+        const unsigned char *stage = rg.ring + st * STAGE_BYTES;
+        for (int j = sub; j < rows; j += RPI) {
+            const float w = rg.w[k * R + j];
+            const float4 *src = reinterpret_cast<const float4 *>(stage + j * row_bytes) + li;
 #pragma unroll
-                for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * 32], w);
-            }
-            slot_out = slot_out + 1 == S ? 0 : slot_out + 1;
+            for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * LPR], w);
         }
+        __syncwarp();   // everyone is done reading the stage before it is refilled
+        if (k + STAGES < nst) produce(k + STAGES);
     }
 #pragma unroll
     for (int sh = LPR; sh < 32; sh <<= 1)
@@ -245,6 +297,7 @@ __device__ __forceinline__ void gather_rows(ACC (&acc)[NV][4], const BwdParams &
         for (int q = 0; q < NV; ++q)
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
+    return __all_sync(FULL, ok);
 }
 
 // Exact rowwise Adagrad on row `row` from the reduced gradient in acc:
@@ -422,10 +475,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nchunks = p.counters[C_NUM_CHUNKS];
-    unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * warp_smem_bytes<NV>(p.chunk);
-    float4 *ring = reinterpret_cast<float4 *>(wsm);
-    int *pb = reinterpret_cast<int *>(wsm + Ring<NV>::S * NV * 32 * 16);
-    float *pw = reinterpret_cast<float *>(pb + p.chunk);
+    WarpRing rg = warp_ring(smem_raw + (threadIdx.x >> 5) * warp_smem_bytes(p.chunk), p.chunk, lane);
     for (int ci = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; ci < nchunks; ci += nwarps) {
         const int l = __ldg(p.chunk_owner + ci);
         const int r = __ldg(p.long_run + l);
@@ -437,7 +487,8 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
         const int t = table_of_key(p.table_offset, p.T, key);
         const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         ACC acc[NV][4];
-        gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, ring, pb, pw);
+        if (!gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, rg) && lane == 0)
+            atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
         ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
         if (sub == 0)
 #pragma unroll
@@ -514,7 +565,7 @@ static constexpr int short_vectors_per_lane(int V) {
 
 template <typename WT, int LPR, int NV>
 static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
-    const size_t csm = (size_t)8 * warp_smem_bytes<NV>(p.chunk);
+    const size_t csm = (size_t)8 * warp_smem_bytes(p.chunk);
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, false>;
         cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
@@ -581,6 +632,7 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.chunk_owner = m->chunk_owner;
     p.partials = a.partials;
     p.arrive = a.arrive;
+    p.status = a.status;
     p.B = a.bt->B;
     p.T = a.tab->T;
     p.D = a.tab->D;

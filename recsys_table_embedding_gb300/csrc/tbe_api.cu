@@ -85,6 +85,8 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     tbe_config c = defaults(cfg);
     if (c.long_run_mode < 0 || c.long_run_mode > 2 || c.hist_mode < 0 || c.hist_mode > 2)
         return TBE_ERR_INVALID_ARGUMENT;
+    // a chunk's lookup table lives in shared memory next to the copy ring
+    if (c.chunk < 32 || c.chunk > 1024) return TBE_ERR_INVALID_ARGUMENT;
     pr->N = bt->N;
     pr->B = bt->B;
     pr->NB = (int64_t)tab->T * bt->B;
@@ -348,6 +350,7 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
     a.eps = eps;
     a.partials = workspace;
     a.arrive = meta->arrive;
+    a.status = dev_status;
     a.max_chunks = pr.max_chunks;
     a.max_long = pr.max_long;
     a.sl_threshold = pr.sl_threshold;

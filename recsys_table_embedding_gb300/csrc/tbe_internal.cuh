@@ -122,6 +122,7 @@ struct BwdArgs {
     float lr, eps;
     void *partials;          // [max_chunks, D] accumulator type
     int32_t *arrive;         // [max_long]
+    int32_t *status;         // caller's device status words
     int64_t max_chunks, max_long;
     int sl_threshold, chunk, long_mode;
 };
