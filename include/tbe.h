@@ -63,7 +63,8 @@ typedef enum tbe_status {
     TBE_ERR_BUFFER_TOO_SMALL = 7,   /* workspace or meta smaller than tbe_query_sizes says */
     TBE_ERR_META = 8,               /* meta not bound, or bound for another problem */
     TBE_ERR_HISTOGRAM_SHAPE = 9,    /* histogram path forced on a shape it does not cover */
-    TBE_ERR_CUDA = 10               /* a kernel launch failed (see cudaGetLastError) */
+    TBE_ERR_CUDA = 10,              /* a kernel launch failed (see cudaGetLastError) */
+    TBE_ERR_SCRATCH_LIMIT = 11      /* batch too large for tbe_preprocess_static's scratch */
 } tbe_status;
 
 typedef enum tbe_dtype { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
@@ -227,6 +228,36 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
                                         void *workspace, size_t workspace_bytes,
                                         int32_t *dev_status, const tbe_config *cfg,
                                         cudaStream_t stream);
+
+/*
+ * The batch inversion of tbe_preprocess without a caller workspace.  The pages
+ * have no counterpart to this call; it is an addition of this library.
+ *
+ * For callers that cannot allocate device memory where they run the batch
+ * inversion: code running inside a device-memory allocator or pool callback
+ * (allocating there would recurse into it), plug-ins that a host framework
+ * hands only fixed input and output buffers, and services that must not grow
+ * their device footprint after start-up.  It allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call.  The caller still passes
+ * the inputs (tables, batch), the output `meta` (bound with tbe_meta_bind)
+ * and `dev_status`; the scratch of the sort and the run-length encoding is a
+ * 4 MiB + 8 KiB device array inside this library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ * Limit: batch->N <= 4,194,304 (2^22) lookups; a larger batch returns
+ * TBE_ERR_SCRATCH_LIMIT before anything is enqueued.  Results equal
+ * tbe_preprocess's.
+ *
+ * The first call on each device looks up the array's address on that device
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the last call's contents (each call re-initialises what it reads):
+ * calls whose work can overlap on the GPU -- on different streams without an
+ * order between them -- race on it and corrupt each other's results, so order
+ * them on one stream.
+ */
+tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_batch *batch, tbe_meta *meta,
+                                 int32_t *dev_status, const tbe_config *cfg, cudaStream_t stream);
 
 /* Which path tbe_forward will take for this problem: 1 generic, 2 histogram. */
 int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);

@@ -4,6 +4,8 @@
 // stream; no device memory is allocated and no host synchronisation happens.
 #include <string.h>
 
+#include <mutex>
+
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -372,6 +374,8 @@ const char *tbe_status_string(tbe_status s) {
     case TBE_ERR_META: return "meta not bound for this problem";
     case TBE_ERR_HISTOGRAM_SHAPE: return "histogram path does not cover this shape";
     case TBE_ERR_CUDA: return "CUDA launch failure";
+    case TBE_ERR_SCRATCH_LIMIT:
+        return "batch larger than tbe_preprocess_static's built-in scratch (at most 4194304 lookups)";
     }
     return "unknown status";
 }
@@ -379,3 +383,73 @@ const char *tbe_status_string(tbe_status s) {
 int32_t tbe_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Batch inversion without a caller workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// batch inversion: code running inside a device-memory allocator or memory
+// pool callback (allocating there would recurse), plug-ins that a host
+// framework hands only fixed input and output buffers, and services that must
+// not grow their device footprint after start-up.  tbe_preprocess_static
+// serves them: the scratch of the radix sort and the run-length encoding is
+// one file-scope device array of this library, so the call allocates nothing.
+// The array occupies STATIC_SCRATCH_BYTES on every GPU that loads the library
+// until the process exits, and bounds the batch at STATIC_SCRATCH_MAX_N
+// lookups.  All calls on a device share the array.
+
+namespace tbe {
+
+constexpr size_t STATIC_SCRATCH_BYTES = (size_t)4 * 1024 * 1024 + 8 * 1024;   // 4 MiB + 8 KiB
+constexpr int64_t STATIC_SCRATCH_MAX_N = (int64_t)1 << 22;                    // 4,194,304 lookups
+constexpr int STATIC_MAX_DEVICES = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+static std::mutex g_static_mu;
+static void *g_static_scratch_ptr[STATIC_MAX_DEVICES];
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static tbe_status static_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= STATIC_MAX_DEVICES) return TBE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || p == nullptr) return TBE_ERR_CUDA;
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return TBE_OK;
+}
+
+}  // namespace tbe
+
+extern "C" tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_batch *batch,
+                                            tbe_meta *meta, int32_t *dev_status,
+                                            const tbe_config *cfg, cudaStream_t stream) {
+    Problem pr;
+    tbe_status st = check_problem(tables, batch, cfg, &pr);
+    if (st != TBE_OK) return st;
+    if (meta == nullptr || dev_status == nullptr) return TBE_ERR_NULL_POINTER;
+    if ((st = check_meta(meta, pr)) != TBE_OK) return st;
+    if (pr.N > STATIC_SCRATCH_MAX_N) return TBE_ERR_SCRATCH_LIMIT;
+    size_t need = sort_workspace_bytes(pr.N, pr.key_bits);
+    if (rle_workspace_bytes(pr.N) > need) need = rle_workspace_bytes(pr.N);
+    if (need > STATIC_SCRATCH_BYTES) return TBE_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if ((st = static_scratch(&scratch)) != TBE_OK) return st;
+    Launch L(stream, cfg);
+    L.num_sms = sm_count();
+    if (pr.path == 2) return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status));
+    // The sort zeroes its digit counts, tile tickets and look-back words, and
+    // the RLE writes its tile counts before reading them, so the contents a
+    // previous call left in the array are never read.
+    st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
+                          (uint32_t)pr.rows_total, dev_status);
+    if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, scratch, dev_status);
+    return finish(L, st);
+}

@@ -33,7 +33,8 @@ _TORCH_DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTED = ("tbe_config_default", "tbe_query_sizes", "tbe_meta_bind", "tbe_forward",
             "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_select_path",
-            "tbe_status_string", "tbe_version")
+            "tbe_status_string", "tbe_version", "tbe_preprocess_static")
+STATIC_SCRATCH_MAX_N = 1 << 22
 
 
 class TbeError(RuntimeError):
@@ -93,6 +94,8 @@ def lib():
         L.tbe_backward_rowwise_adagrad.restype = i32
         L.tbe_backward_rowwise_adagrad.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float,
                                                    P, ctypes.c_size_t, P, P, P]
+        L.tbe_preprocess_static.restype = i32
+        L.tbe_preprocess_static.argtypes = [P, P, P, P, P, P]
         L.tbe_select_path.restype = i32
         L.tbe_select_path.argtypes = [P, P, P]
         L.tbe_status_string.restype = ctypes.c_char_p
@@ -204,6 +207,15 @@ def tbe_preprocess(tables: Tables, batch: Batch, meta: Meta, workspace: torch.Te
     _check(lib().tbe_preprocess(ctypes.byref(tables.c), ctypes.byref(batch.c), ctypes.byref(meta.c),
                                 workspace.data_ptr(), workspace.numel(), dev_status.data_ptr(),
                                 ctypes.byref(cfg) if cfg else None, _stream(stream)))
+
+
+def tbe_preprocess_static(tables: Tables, batch: Batch, meta: Meta, dev_status: torch.Tensor,
+                          cfg: Optional[tbe_config] = None, stream=None):
+    """Batch inversion without a workspace, for callers that cannot allocate
+    device memory at this point (see include/tbe.h); at most 2^22 lookups."""
+    _check(lib().tbe_preprocess_static(ctypes.byref(tables.c), ctypes.byref(batch.c),
+                                       ctypes.byref(meta.c), dev_status.data_ptr(),
+                                       ctypes.byref(cfg) if cfg else None, _stream(stream)))
 
 
 def tbe_backward_rowwise_adagrad(tables: Tables, batch: Batch, momentum: torch.Tensor,
