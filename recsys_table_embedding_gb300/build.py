@@ -55,6 +55,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "-I", CSRC, "--expt-relaxed-constexpr", "-Xcompiler", "-Wall"]
     if os.environ.get("TBE_PTXAS_VERBOSE"):
         flags += ["-Xptxas", "-v"]
+    # tuning knobs (-DTBE_FWD_ROWS=...), e.g. for launch-shape sweeps
+    flags += os.environ.get("TBE_NVCC_DEFINES", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")

@@ -163,7 +163,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 
 constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = 4096;
-constexpr long long BAR_WAIT_LIMIT = 1ll << 26;
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -171,17 +170,6 @@ __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void bar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
 }
 // global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned)
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -273,12 +261,15 @@ __device__ __forceinline__ bool gather_rows(ACC (&acc)[NV][4], const BwdParams &
         const int st = k % STAGES;
         const uint32_t bar = rg.bar0 + 8 * st;
         const uint32_t par = (rg.phase >> st) & 1u;
-        long long spins = 0;
-        while (!bar_try_wait(bar, par))
-            if (++spins > BAR_WAIT_LIMIT) {
-                ok = false;
-                break;
-            }
+        if (!mbar_wait_bounded(bar, par)) {
+            // stop issuing: give the copies still in flight (stages k+1 ..
+            // k+STAGES-1 of this range) one more bounded wait before the
+            // caller flags the failure and ends the warp's work
+            for (int k2 = k + 1; k2 < nst && k2 < k + STAGES; ++k2)
+                mbar_wait_bounded(rg.bar0 + 8 * (k2 % STAGES), (rg.phase >> (k2 % STAGES)) & 1u);
+            ok = false;
+            break;
+        }
         rg.phase ^= 1u << st;
         const int rows = min(R, n - k * R);
         const unsigned char *stage = rg.ring + st * STAGE_BYTES;
@@ -487,8 +478,10 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
         const int t = table_of_key(p.table_offset, p.T, key);
         const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         ACC acc[NV][4];
-        if (!gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, rg) && lane == 0)
-            atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
+        if (!gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, rg)) {
+            if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
+            return;   // results are invalid (flagged); issue nothing more
+        }
         ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
         if (sub == 0)
 #pragma unroll

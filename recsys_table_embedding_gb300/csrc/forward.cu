@@ -16,6 +16,8 @@
 // the pooled row is written once.  When preprocessing runs in the forward,
 // the same pass writes the linearised key and the sort payload of every
 // lookup (coalesced, in position order).
+#include <type_traits>
+
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -41,43 +43,52 @@ struct FwdParams {
     int payload_pos;
 };
 
-__device__ __forceinline__ void accum_vec(double (&a)[4], const uint4 v, float w) {
-    const float *f = reinterpret_cast<const float *>(&v);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] = fma((double)w, (double)f[e], a[e]);
-}
-__device__ __forceinline__ void accum_vec(float (&a)[8], const uint4 v, float w, __half) {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float2 f = __half22float2(h[e]);
-        a[2 * e] = fmaf(w, f.x, a[2 * e]);
-        a[2 * e + 1] = fmaf(w, f.y, a[2 * e + 1]);
+// A VB-byte vector of a weight row (VB = 8 or 16) as 32-bit words.
+template <int VB> struct Vec {
+    uint32_t v[VB / 4];
+};
+template <int VB> __device__ __forceinline__ Vec<VB> ldg_vec(const void *p) {
+    Vec<VB> r;
+    if constexpr (VB == 16) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(p));
+        r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[3] = q.w;
+    } else {
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(p));
+        r.v[0] = q.x; r.v[1] = q.y;
     }
+    return r;
 }
-__device__ __forceinline__ void accum_vec(float (&a)[8], const uint4 v, float w, __nv_bfloat16) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+
+// acc[e] += w * element e of the vector (FP64 accumulators for FP32 tables)
+template <typename WT, int VB, typename ACC>
+__device__ __forceinline__ void accum(ACC (&a)[VB / sizeof(WT)], const Vec<VB> &x, float w) {
+    constexpr int NW = VB / 4;
+    if constexpr (sizeof(WT) == 4) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(h[e]);
-        a[2 * e] = fmaf(w, f.x, a[2 * e]);
-        a[2 * e + 1] = fmaf(w, f.y, a[2 * e + 1]);
+        for (int e = 0; e < NW; ++e) a[e] = fma((double)w, (double)__uint_as_float(x.v[e]), a[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < NW; ++e) {
+            float2 f;
+            if constexpr (std::is_same<WT, __half>::value)
+                f = __half22float2(*reinterpret_cast<const __half2 *>(&x.v[e]));
+            else
+                f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.v[e]));
+            a[2 * e] = fmaf(w, f.x, a[2 * e]);
+            a[2 * e + 1] = fmaf(w, f.y, a[2 * e + 1]);
+        }
     }
 }
 
-template <typename WT>
-__device__ __forceinline__ void accum(typename WTraits<WT>::acc (&a)[WTraits<WT>::VEC], uint4 v,
-                                      float w) {
-    if constexpr (sizeof(WT) == 4) accum_vec(a, v, w);
-    else accum_vec(a, v, w, WT());
-}
-
-__device__ __forceinline__ void store_out(float *o, const double (&a)[4]) {
-    __stcs(reinterpret_cast<float4 *>(o), make_float4((float)a[0], (float)a[1], (float)a[2], (float)a[3]));
-}
-__device__ __forceinline__ void store_out(float *o, const float (&a)[8]) {
-    __stcs(reinterpret_cast<float4 *>(o), make_float4(a[0], a[1], a[2], a[3]));
-    __stcs(reinterpret_cast<float4 *>(o) + 1, make_float4(a[4], a[5], a[6], a[7]));
+template <int VEC, typename ACC> __device__ __forceinline__ void store_out(float *o, const ACC (&a)[VEC]) {
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < VEC / 4; ++i)
+            __stcs(reinterpret_cast<float4 *>(o) + i,
+                   make_float4((float)a[4 * i], (float)a[4 * i + 1], (float)a[4 * i + 2], (float)a[4 * i + 3]));
+    } else {
+        __stcs(reinterpret_cast<float2 *>(o), make_float2((float)a[0], (float)a[1]));
+    }
 }
 
 __device__ __forceinline__ int warp_sum_i(int v) {
@@ -86,10 +97,10 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     return v;
 }
 
-template <typename WT, int LPR, int NV, int U>
+template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED>
 __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
     using ACC = typename WTraits<WT>::acc;
-    constexpr int VEC = WTraits<WT>::VEC;
+    constexpr int VEC = VB / (int)sizeof(WT);   // elements per lane vector
     constexpr int RPI = 32 / LPR;
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -106,7 +117,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
             if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
             start = end = 0;   // malformed bag: empty
         }
-        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
+        const bool wt = WEIGHTED && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         const WT *Wt = reinterpret_cast<const WT *>(p.W) + row0 * p.D + li * VEC;
         ACC acc[NV][VEC];
 #pragma unroll
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
             }
             const unsigned vmask = __ballot_sync(FULL, valid);
             for (int j = 0; j < n; j += RPI * U) {
-                uint4 v[U][NV];
+                Vec<VB> v[U][NV];
                 float wv[U];
                 bool ok[U];
 #pragma unroll
@@ -139,19 +150,19 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
                     const int k = j + u * RPI + sub;
                     const int src = k & 31;
                     const int32_t ik = __shfl_sync(FULL, idx, src);
-                    wv[u] = __shfl_sync(FULL, w, src);
+                    wv[u] = WEIGHTED ? __shfl_sync(FULL, w, src) : 1.f;
                     ok[u] = k < n && ((vmask >> src) & 1u);
                     if (ok[u]) {
                         const WT *r = Wt + (int64_t)ik * p.D;
 #pragma unroll
-                        for (int q = 0; q < NV; ++q) v[u][q] = ldg_v4(r + q * LPR * VEC);
+                        for (int q = 0; q < NV; ++q) v[u][q] = ldg_vec<VB>(r + q * LPR * VEC);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     if (ok[u])
 #pragma unroll
-                        for (int q = 0; q < NV; ++q) accum<WT>(acc[q], v[u][q], wv[u]);
+                        for (int q = 0; q < NV; ++q) accum<WT, VB>(acc[q], v[u][q], wv[u]);
             }
         }
 #pragma unroll
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
         if (sub == 0) {
             float *o = p.out + (b * p.T + t) * (int64_t)p.D + li * VEC;
 #pragma unroll
-            for (int q = 0; q < NV; ++q) store_out(o + q * LPR * VEC, acc[q]);
+            for (int q = 0; q < NV; ++q) store_out<VEC>(o + q * LPR * VEC, acc[q]);
         }
     }
     oob = warp_sum_i(oob);
@@ -228,30 +239,41 @@ static int grid_for(K kernel, int threads, int64_t work_warps, int num_sms) {
     return (int)(g < 1 ? 1 : g);
 }
 
-template <typename WT, int LPR, int NV>
+#ifndef TBE_FWD_ROWS
+#define TBE_FWD_ROWS 4   // weight rows in flight per warp (4, 8, 16 measured; 4 best)
+#endif
+
+template <typename WT, int VB, int LPR, int NV>
 static void fwd_launch(Launch &L, const FwdParams &p) {
+    // rows in flight per warp: 32/LPR per step, U steps -> TBE_FWD_ROWS rows,
+    // with at most 32 registers of loaded data per lane
     constexpr int RPI = 32 / LPR;
-    constexpr int U0 = RPI >= 8 ? 1 : (8 / RPI);
-    constexpr int U = (U0 * NV > 8) ? (8 / NV > 0 ? 8 / NV : 1) : U0;
-    auto k = tbe_fwd_kernel<WT, LPR, NV, U>;
+    constexpr int U0 = RPI >= TBE_FWD_ROWS ? 1 : (TBE_FWD_ROWS / RPI);
+    constexpr int WORDS = NV * VB / 4;
+    constexpr int U = (U0 * WORDS > 32) ? (32 / WORDS > 0 ? 32 / WORDS : 1) : U0;
+    auto k = p.psw != nullptr ? tbe_fwd_kernel<WT, VB, LPR, NV, U, true>
+                              : tbe_fwd_kernel<WT, VB, LPR, NV, U, false>;
     const int grid = grid_for(k, 256, p.NB, L.num_sms);
     L.before("tbe_fwd_gather");
     k<<<grid, 256, 0, L.stream>>>(p);
     L.after();
 }
 
+// Rows are read as 16-byte lane vectors: a warp instruction covers 512 bytes
+// (fewer, larger requests measured faster than 8-byte vectors on this path).
 template <typename WT>
-static bool fwd_dispatch(Launch &L, const FwdParams &p, RowPlan rp) {
+static bool fwd_dispatch(Launch &L, const FwdParams &p, int row_bytes) {
+    const RowPlan rp = row_plan(row_bytes / (int)sizeof(WT), (int)sizeof(WT));
     switch (rp.lpr * 10 + rp.nv) {
-    case 11: fwd_launch<WT, 1, 1>(L, p); return true;
-    case 21: fwd_launch<WT, 2, 1>(L, p); return true;
-    case 41: fwd_launch<WT, 4, 1>(L, p); return true;
-    case 81: fwd_launch<WT, 8, 1>(L, p); return true;
-    case 161: fwd_launch<WT, 16, 1>(L, p); return true;
-    case 321: fwd_launch<WT, 32, 1>(L, p); return true;
-    case 322: fwd_launch<WT, 32, 2>(L, p); return true;
-    case 323: fwd_launch<WT, 32, 3>(L, p); return true;
-    case 324: fwd_launch<WT, 32, 4>(L, p); return true;
+    case 11: fwd_launch<WT, 16, 1, 1>(L, p); return true;
+    case 21: fwd_launch<WT, 16, 2, 1>(L, p); return true;
+    case 41: fwd_launch<WT, 16, 4, 1>(L, p); return true;
+    case 81: fwd_launch<WT, 16, 8, 1>(L, p); return true;
+    case 161: fwd_launch<WT, 16, 16, 1>(L, p); return true;
+    case 321: fwd_launch<WT, 16, 32, 1>(L, p); return true;
+    case 322: fwd_launch<WT, 16, 32, 2>(L, p); return true;
+    case 323: fwd_launch<WT, 16, 32, 3>(L, p); return true;
+    case 324: fwd_launch<WT, 16, 32, 4>(L, p); return true;
     default: return false;
     }
 }
@@ -286,10 +308,11 @@ tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
     FwdParams p = make_params(tab, bt, out, keys, vals, bag_of, sentinel, status);
     if (p.NB == 0) return TBE_OK;
     bool ok = false;
+    if (!row_plan(tab->D, tab->dtype == TBE_F32 ? 4 : 2).ok) return TBE_ERR_UNSUPPORTED_DIM;
     switch (tab->dtype) {
-    case TBE_F32: ok = fwd_dispatch<float>(L, p, row_plan(tab->D, 4)); break;
-    case TBE_F16: ok = fwd_dispatch<__half>(L, p, row_plan(tab->D, 2)); break;
-    case TBE_BF16: ok = fwd_dispatch<__nv_bfloat16>(L, p, row_plan(tab->D, 2)); break;
+    case TBE_F32: ok = fwd_dispatch<float>(L, p, tab->D * 4); break;
+    case TBE_F16: ok = fwd_dispatch<__half>(L, p, tab->D * 2); break;
+    case TBE_BF16: ok = fwd_dispatch<__nv_bfloat16>(L, p, tab->D * 2); break;
     default: return TBE_ERR_UNSUPPORTED_DTYPE;
     }
     return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;

@@ -37,7 +37,6 @@ constexpr int HF_THREADS = 256;
 constexpr int HB_THREADS = 256;
 constexpr int HB_KBAGS = 64;    // bags per backward K step
 constexpr int CNT_STRIDE = HE + 1;
-constexpr long long WAIT_LIMIT = 1ll << 26;
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -51,22 +50,9 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // bounded wait on the phase with the given parity; false on timeout
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (long long i = 0; i < WAIT_LIMIT; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    return mbar_wait_bounded(smem_u32(bar), parity);
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

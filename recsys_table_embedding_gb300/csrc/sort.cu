@@ -16,9 +16,9 @@
 //     running prefix.  The tile is reordered by digit in shared memory and
 //     written out, so each digit's run of pairs lands contiguously.
 //  The look-back status word packs a 2-bit state and a 30-bit count (so
-//  N < 2^30).  Every wait is bounded: after MAX_SPINS polls the CTA sets
-//  TBE_FLAG_SORT_TIMEOUT in the status word and carries on (the sort output
-//  is then invalid, which the flag reports).
+//  N < 2^30).  Every wait is bounded: after WAIT_LIMIT_NS of polling the CTA
+//  sets TBE_FLAG_SORT_TIMEOUT in the status word and carries on (the sort
+//  output is then invalid, which the flag reports).
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -33,7 +33,6 @@ constexpr uint32_t ST_AGG = 1u << 30;
 constexpr uint32_t ST_INC = 2u << 30;
 constexpr uint32_t ST_MASK = (1u << 30) - 1;
 constexpr int MAX_PASSES = 4;
-constexpr long long MAX_SPINS = 1ll << 24;
 
 static int num_passes(int key_bits) { return (key_bits + RADIX_BITS - 1) / RADIX_BITS; }
 
@@ -186,12 +185,14 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
         } else {
             st_relaxed_u32(st, ST_AGG | sum);
             int64_t j = tile - 1;
-            long long spins = 0;
+            uint64_t t0 = 0;
             while (true) {
                 const uint32_t s = ld_relaxed_u32(status + j * RADIX + d);
                 const uint32_t f = s & ~ST_MASK;
                 if (f == 0) {
-                    if (++spins > MAX_SPINS) {
+                    const uint64_t now = global_ns();
+                    if (t0 == 0) t0 = now;
+                    else if (now - t0 > WAIT_LIMIT_NS) {
                         atomicOr(err, TBE_FLAG_SORT_TIMEOUT);
                         break;
                     }

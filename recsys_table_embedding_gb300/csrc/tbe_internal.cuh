@@ -57,6 +57,37 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Every device-side wait in this library gives up after this long (wall
+// clock, from the %globaltimer nanosecond counter), sets a status flag and
+// stops issuing work.  Waits normally end within microseconds.
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the completion of the mbarrier phase with the given parity
+// (shared-memory address `bar`).  False if WAIT_LIMIT_NS passed first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        const uint64_t now = global_ns();
+        if (i == 0) t0 = now;
+        else if (now - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+
 // Table of a linearised key: largest t with table_offset[t] <= key (T small).
 __device__ __forceinline__ int table_of_key(const int64_t *table_offset, int T, int64_t key) {
     int lo = 0, hi = T;   // answer in [lo, hi)
