@@ -562,12 +562,16 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, false>;
         cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+        cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
         L.before("tbe_bwd_grad_accum");
         kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
         L.after();
     } else {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, true>;
         cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+        cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
         L.before("tbe_bwd_fused_long");
         kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
         L.after();

@@ -36,7 +36,7 @@ constexpr int HT_BAGS = 128;    // bags per forward tile (M)
 constexpr int HF_THREADS = 256;
 constexpr int HB_THREADS = 256;
 constexpr int HB_KBAGS = 64;    // bags per backward K step
-constexpr int CNT_STRIDE = HE + 1;
+constexpr int CNT_STRIDE = HE / 2 + 1;   // 16-bit count pairs per bag, +1 word against bank conflicts
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -146,10 +146,14 @@ struct HistFwdParams {
     int do_mma;
 };
 
+constexpr int STG_PITCH = 36;   // floats per staged output row (32 + 4 against bank conflicts)
+
 struct HistFwdSmem {
+    // A and cnt are contiguous: after the MMA, they serve as the staging
+    // buffer of the output ([128 bags][STG_PITCH] floats)
     alignas(1024) unsigned char A[HT_BAGS * 128];   // counts as FP16, [128 bags][64 rows]
+    uint32_t cnt[HT_BAGS * CNT_STRIDE];             // two 16-bit counts per word
     alignas(1024) unsigned char Bm[128 * 128];      // W_t^T, [D][64 rows]
-    uint32_t cnt[HT_BAGS * CNT_STRIDE];
     int32_t offs[HT_BAGS + 1];
     uint64_t mbar;
     uint32_t tmem_base;
@@ -241,23 +245,26 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
                     const int mid = (lo + hi) >> 1;
                     if (S.offs[mid] <= pos) lo = mid; else hi = mid;
                 }
-                if (idx[u] >= 0 && (int64_t)idx[u] < E) atomicAdd(&S.cnt[lo * CNT_STRIDE + idx[u]], 1u);
-                else ++oob;
+                if (idx[u] >= 0 && (int64_t)idx[u] < E)
+                    atomicAdd(&S.cnt[lo * CNT_STRIDE + (idx[u] >> 1)], 1u << ((idx[u] & 1) * 16));
+                else
+                    ++oob;
             }
         }
         __syncthreads();
         // counts -> FP16 A operand (+ saved histogram); thread = (row r, half h)
         {
             const int r = tid & (HT_BAGS - 1), h = tid >> 7;
-            int over = 0;
+            // a 16-bit count could wrap only in a bag of more than 65535 lookups
+            int over = h == 0 && r < nb && S.offs[r + 1] - S.offs[r] > 65535;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c = h * 4 + cc;
                 uint32_t packed[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t c0 = S.cnt[r * CNT_STRIDE + c * 8 + 2 * q];
-                    const uint32_t c1 = S.cnt[r * CNT_STRIDE + c * 8 + 2 * q + 1];
+                    const uint32_t pair = S.cnt[r * CNT_STRIDE + c * 4 + q];
+                    const uint32_t c0 = pair & 0xFFFFu, c1 = pair >> 16;
                     over |= (c0 > 2048u) | (c1 > 2048u);
                     __half2 hv = __halves2half2(__uint2half_rn(c0), __uint2half_rn(c1));
                     packed[q] = *reinterpret_cast<uint32_t *>(&hv);
@@ -293,24 +300,38 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
             if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_MMA_TIMEOUT);
             alive = false;
         } else {
-            // epilogue: warp w reads TMEM lanes 32*(w%4).., column half w/4
-            const int q = warp & 3, half = warp >> 2;
-            const int row = q * 32 + lane;
-            const int ncol = p.D >> 1;
-            float *o = p.out + (b0 + row) * (int64_t)p.T * p.D + (int64_t)t * p.D + half * ncol;
+            // epilogue, 32 columns per pass: TMEM -> shared staging (warp w
+            // reads lanes 32*(w%4).. of columns +16*(w/4)), then full output
+            // row segments written by consecutive threads (coalesced)
+            static_assert(HT_BAGS * STG_PITCH * 4 <= HT_BAGS * 128 + HT_BAGS * CNT_STRIDE * 4,
+                          "output staging fits in A + cnt");
+            float *stg = reinterpret_cast<float *>(S.A);
+            const int q = warp & 3, hh = warp >> 2;
+            for (int pc = 0; pc * 32 < p.D; ++pc) {
+                const int ncols = min(32, p.D - pc * 32);
+                if (hh * 16 < ncols) {   // warp-uniform
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                if (c8 * 8 >= ncol) break;
-                uint32_t r[8];
-                tmem_ld8(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * ncol + c8 * 8), r);
-                tmem_wait_ld();
-                if (row < nb) {
-                    float4 *o4 = reinterpret_cast<float4 *>(o + c8 * 8);
-                    __stcs(o4, make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                           __uint_as_float(r[2]), __uint_as_float(r[3])));
-                    __stcs(o4 + 1, make_float4(__uint_as_float(r[4]), __uint_as_float(r[5]),
-                                               __uint_as_float(r[6]), __uint_as_float(r[7])));
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        uint32_t r[8];
+                        tmem_ld8(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(pc * 32 + hh * 16 + c8 * 8), r);
+                        tmem_wait_ld();
+                        float4 *dst = reinterpret_cast<float4 *>(stg + (q * 32 + lane) * STG_PITCH + hh * 16 + c8 * 8);
+                        dst[0] = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
+                                             __uint_as_float(r[2]), __uint_as_float(r[3]));
+                        dst[1] = make_float4(__uint_as_float(r[4]), __uint_as_float(r[5]),
+                                             __uint_as_float(r[6]), __uint_as_float(r[7]));
+                    }
                 }
+                __syncthreads();
+                const int per_row = ncols / 4;
+                for (int i = tid; i < HT_BAGS * per_row; i += HF_THREADS) {
+                    const int row = i / per_row, c4 = i - row * per_row;
+                    if (row < nb)
+                        __stcs(reinterpret_cast<float4 *>(p.out + (b0 + row) * (int64_t)p.T * p.D +
+                                                          (int64_t)t * p.D + pc * 32) + c4,
+                               *reinterpret_cast<const float4 *>(stg + row * STG_PITCH + c4 * 4));
+                }
+                __syncthreads();
             }
         }
         tc_fence_before();
@@ -396,6 +417,32 @@ __global__ void __launch_bounds__(HB_THREADS) tbe_hist_bwd_kernel(const HistBwdP
     float mycnt = 0.f;
     int over = 0;
 
+    // Operands of one K step held in registers: 32 gradient values of one
+    // column d (8-bag chunks jc, jc+2, jc+4, jc+6) and 16 counts of one row e
+    // (chunks je, je+4).  The next step's loads are issued before this step's
+    // barrier and MMA issue, so their latency overlaps them.
+    const int gd = tid & 127, gjc = tid >> 7;
+    const int he = tid & 63, hjc = tid >> 6;
+    float gv[32];
+    uint16_t hv[16];
+    auto load_step = [&](int i) {
+        const int64_t k0 = bb + (int64_t)i * HB_KBAGS;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+                const int64_t b = k0 + (gjc + 2 * cc) * 8 + z;
+                gv[cc * 8 + z] = (gd < p.D && b < be) ? __ldg(p.G + b * TD + (int64_t)t * p.D + gd) : 0.f;
+            }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+                const int64_t b = k0 + (hjc + 4 * cc) * 8 + z;
+                hv[cc * 8 + z] = b < be ? __ldg(p.hist + ((int64_t)t * p.B + b) * HE + he) : (uint16_t)0;
+            }
+    };
+    if (nsteps > 0) load_step(0);
     for (int i = 0; i < nsteps && alive; ++i) {
         const int st = i & 1;
         HistBwdStage &SG = S.st[st];
@@ -408,58 +455,41 @@ __global__ void __launch_bounds__(HB_THREADS) tbe_hist_bwd_kernel(const HistBwdP
             ph[st] ^= 1;
             tc_fence_after();
         }
-        const int64_t k0 = bb + (int64_t)i * HB_KBAGS;
-        // G^T hi/lo: thread = (d, chunk group); 8 consecutive bags per 16-byte chunk
-        {
-            const int d = tid & 127, jc = tid >> 7;
+        // G^T hi/lo into the A tiles: 8 consecutive bags per 16-byte chunk
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = jc + 2 * cc;
-                uint32_t hw[4], lw[4];
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c = gjc + 2 * cc;
+            uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float g2[2];
-#pragma unroll
-                    for (int z = 0; z < 2; ++z) {
-                        const int64_t b = k0 + c * 8 + 2 * q + z;
-                        g2[z] = (d < p.D && b < be)
-                                    ? __ldg(p.G + b * TD + (int64_t)t * p.D + d)
-                                    : 0.f;
-                        over |= fabsf(g2[z]) > 65504.f;
-                    }
-                    const __half h0 = __float2half_rn(g2[0]), h1 = __float2half_rn(g2[1]);
-                    const __half l0 = __float2half_rn(g2[0] - __half2float(h0));
-                    const __half l1 = __float2half_rn(g2[1] - __half2float(h1));
-                    __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-                    hw[q] = *reinterpret_cast<uint32_t *>(&hh);
-                    lw[q] = *reinterpret_cast<uint32_t *>(&ll);
-                }
-                const uint32_t off = (uint32_t)(d * 128 + ((c ^ (d & 7)) << 4));
-                *reinterpret_cast<uint4 *>(SG.Ahi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(SG.Alo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            for (int q = 0; q < 4; ++q) {
+                const float g0 = gv[cc * 8 + 2 * q], g1 = gv[cc * 8 + 2 * q + 1];
+                over |= (fabsf(g0) > 65504.f) | (fabsf(g1) > 65504.f);
+                const __half h0 = __float2half_rn(g0), h1 = __float2half_rn(g1);
+                const __half l0 = __float2half_rn(g0 - __half2float(h0));
+                const __half l1 = __float2half_rn(g1 - __half2float(h1));
+                __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+                hw[q] = *reinterpret_cast<uint32_t *>(&hh);
+                lw[q] = *reinterpret_cast<uint32_t *>(&ll);
             }
+            const uint32_t off = (uint32_t)(gd * 128 + ((c ^ (gd & 7)) << 4));
+            *reinterpret_cast<uint4 *>(SG.Ahi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(SG.Alo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        // H^T: thread = (row e, chunk group); counts also summed per row
-        {
-            const int e = tid & 63, jc = tid >> 6;
+        // H^T into the B tile; counts summed per row
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = jc + 4 * cc;
-                uint16_t hv[8];
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = hjc + 4 * cc;
+            const uint16_t *h8 = hv + cc * 8;
 #pragma unroll
-                for (int z = 0; z < 8; ++z) {
-                    const int64_t b = k0 + c * 8 + z;
-                    hv[z] = b < be ? __ldg(p.hist + ((int64_t)t * p.B + b) * HE + e) : (uint16_t)0;
-                    mycnt += __half2float(__ushort_as_half(hv[z]));
-                }
-                uint4 v;
-                v.x = hv[0] | ((uint32_t)hv[1] << 16);
-                v.y = hv[2] | ((uint32_t)hv[3] << 16);
-                v.z = hv[4] | ((uint32_t)hv[5] << 16);
-                v.w = hv[6] | ((uint32_t)hv[7] << 16);
-                *reinterpret_cast<uint4 *>(SG.Bh + e * 128 + ((c ^ (e & 7)) << 4)) = v;
-            }
+            for (int z = 0; z < 8; ++z) mycnt += __half2float(__ushort_as_half(h8[z]));
+            uint4 v;
+            v.x = h8[0] | ((uint32_t)h8[1] << 16);
+            v.y = h8[2] | ((uint32_t)h8[3] << 16);
+            v.z = h8[4] | ((uint32_t)h8[5] << 16);
+            v.w = h8[6] | ((uint32_t)h8[7] << 16);
+            *reinterpret_cast<uint4 *>(SG.Bh + he * 128 + ((c ^ (he & 7)) << 4)) = v;
         }
+        if (i + 1 < nsteps) load_step(i + 1);
         fence_async_smem();
         __syncthreads();
         if (tid == 0 && alive) {
@@ -605,10 +635,13 @@ static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_ba
     p.do_mma = do_mma;
     const size_t smem = fwd_smem();
     cudaFuncSetAttribute(tbe_hist_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tbe_hist_fwd_kernel, HF_THREADS, smem);
+    cudaFuncSetAttribute(tbe_hist_fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    // CTAs per SM: shared memory (227 KB usable, 1 KB reserved per CTA) and
+    // TMEM (512 columns, 128 per CTA) both allow 4 (64 registers x 256 threads allow 4)
+    int per_sm = (int)((227 * 1024) / (smem + 1024));
+    if (per_sm > 4) per_sm = 4;
     if (per_sm < 1) per_sm = 1;
-    if (per_sm > 3) per_sm = 3;   // TMEM: 3 x 128 columns per SM
     int64_t grid = (int64_t)L.num_sms * per_sm;
     if (grid > p.tiles_total) grid = p.tiles_total;
     p.tiles_per_cta = (p.tiles_total + grid - 1) / grid;
@@ -660,6 +693,8 @@ tbe_status launch_hist_backward(Launch &L, const tbe_tables *tab, const tbe_batc
     L.after();
     const size_t smem = bwd_smem();
     cudaFuncSetAttribute(tbe_hist_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(tbe_hist_bwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     L.before("tbe_hist_bwd_umma");
     tbe_hist_bwd_kernel<<<(unsigned)(tab->T * p.S), HB_THREADS, smem, L.stream>>>(p);
     L.after();

@@ -288,6 +288,8 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
     static_assert(sizeof(PassSmem) < 227 * 1024, "pass shared memory");
     cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
+    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     const uint32_t *ki = keys_a, *vi = vals_a;
     uint32_t *ko = keys_b, *vo = vals_b;
     for (int ps = 0; ps < passes; ++ps) {
