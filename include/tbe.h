@@ -241,7 +241,7 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
  * cudaMalloc, cudaFree or allocating library call.  The caller still passes
  * the inputs (tables, batch), the output `meta` (bound with tbe_meta_bind)
  * and `dev_status`; the scratch of the sort and the run-length encoding is a
- * 4 MiB + 8 KiB device array inside this library, which every GPU that loads
+ * 8 MiB + 64 KiB device array inside this library, which every GPU that loads
  * the library holds until the process exits.
  *
  * Limit: batch->N <= 4,194,304 (2^22) lookups; a larger batch returns

@@ -1,18 +1,19 @@
 // Stable LSD radix sort of (key, payload) pairs: the sort step of the batch
 // inversion (FBTriton TBE redesign, accesspath.com, "transpose_embedding_input";
 // decision checklist item 6: int32 keys halve the sort-key width).  Only the
-// significant key bits are sorted: ceil(key_bits / 8) passes of 8 bits.
+// significant key bits are sorted, in ceil(key_bits / 9) passes of at most
+// 9 bits (512 buckets): 26-bit keys take 3 passes.
 //
 // Design (onesweep: one read and one write of the pairs per pass, digit
 // prefixes across tiles by decoupled look-back):
 //  1. one histogram kernel counts every pass's digits at once and zeroes the
-//     look-back state; a 256-thread kernel per pass turns counts into bucket
+//     look-back state; a 512-thread kernel per pass turns counts into bucket
 //     starts;
 //  2. per pass, CTAs take tiles in ticket order (an atomic counter, so a
 //     CTA only ever waits for tiles that CTAs already running hold).  A tile
 //     of 4096 pairs is ranked stably inside the CTA (per-warp match_any
 //     ranking in input order, then warp prefixes), each digit's tile count is
-//     published, and thread d looks back over earlier tiles for digit d's
+//     published, and thread d (one per bucket) looks back over earlier tiles for digit d's
 //     running prefix.  The tile is reordered by digit in shared memory and
 //     written out, so each digit's run of pairs lands contiguously.
 //  The look-back status word packs a 2-bit state and a 30-bit count (so
@@ -23,8 +24,8 @@
 
 namespace tbe {
 
-constexpr int RADIX_BITS = 8;
-constexpr int RADIX = 256;
+constexpr int MAX_DIGIT_BITS = 9;
+constexpr int RADIX = 1 << MAX_DIGIT_BITS;   // buckets per pass (digits use <= 9 bits)
 constexpr int SORT_THREADS = 512;
 constexpr int SORT_WARPS = SORT_THREADS / 32;
 constexpr int SORT_IPT = 8;
@@ -34,12 +35,16 @@ constexpr uint32_t ST_INC = 2u << 30;
 constexpr uint32_t ST_MASK = (1u << 30) - 1;
 constexpr int MAX_PASSES = 4;
 
-static int num_passes(int key_bits) { return (key_bits + RADIX_BITS - 1) / RADIX_BITS; }
+static int num_passes(int key_bits) { return (key_bits + MAX_DIGIT_BITS - 1) / MAX_DIGIT_BITS; }
+static int digit_bits(int key_bits) {
+    const int p = num_passes(key_bits);
+    return p > 0 ? (key_bits + p - 1) / p : 0;
+}
 
 struct SortWs {
-    uint32_t *hist;        // [MAX_PASSES][256] digit counts, then bucket starts
+    uint32_t *hist;        // [MAX_PASSES][RADIX] digit counts, then bucket starts
     uint32_t *tickets;     // [MAX_PASSES] tile tickets
-    uint32_t *status;      // [MAX_PASSES][ntiles][256] look-back words
+    uint32_t *status;      // [MAX_PASSES][ntiles][RADIX] look-back words
     int64_t ntiles;
 };
 
@@ -62,8 +67,9 @@ size_t sort_workspace_bytes(int64_t N, int key_bits) {
 }
 
 __global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t *__restrict__ keys, int64_t N,
-                                                         int passes, uint32_t *hist,
+                                                         int passes, int bits, uint32_t *hist,
                                                          uint32_t *zero, int64_t zero_words) {
+    const uint32_t mask = (1u << bits) - 1;
     __shared__ uint32_t sh[MAX_PASSES * RADIX];
     for (int i = threadIdx.x; i < MAX_PASSES * RADIX; i += blockDim.x) sh[i] = 0;
     __syncthreads();
@@ -76,12 +82,12 @@ __global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t *__restr
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             for (int ps = 0; ps < passes; ++ps)
-                atomicAdd(&sh[ps * RADIX + ((kk[e] >> (ps * RADIX_BITS)) & (RADIX - 1))], 1u);
+                atomicAdd(&sh[ps * RADIX + ((kk[e] >> (ps * bits)) & mask)], 1u);
     }
     for (int64_t i = N4 * 4 + tid; i < N; i += stride) {
         const uint32_t k = __ldg(keys + i);
         for (int ps = 0; ps < passes; ++ps)
-            atomicAdd(&sh[ps * RADIX + ((k >> (ps * RADIX_BITS)) & (RADIX - 1))], 1u);
+            atomicAdd(&sh[ps * RADIX + ((k >> (ps * bits)) & mask)], 1u);
     }
     for (int64_t i = tid; i < zero_words; i += stride) zero[i] = 0;
     __syncthreads();
@@ -89,8 +95,8 @@ __global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t *__restr
         if (sh[i]) atomicAdd(&hist[i], sh[i]);
 }
 
-// Exclusive scan of one pass's 256 digit counts into bucket starts, in place.
-__global__ void __launch_bounds__(256) radix_bucket_kernel(uint32_t *hist) {
+// Exclusive scan of one pass's RADIX digit counts into bucket starts, in place.
+__global__ void __launch_bounds__(RADIX) radix_bucket_kernel(uint32_t *hist) {
     __shared__ uint32_t s[RADIX];
     uint32_t *h = hist + blockIdx.x * RADIX;
     const int d = threadIdx.x;
@@ -125,7 +131,7 @@ struct PassSmem {
 __global__ void __launch_bounds__(SORT_THREADS, 2)
 radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
                       uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t N,
-                      int shift, const uint32_t *__restrict__ bucket, uint32_t *status,
+                      int shift, uint32_t mask, const uint32_t *__restrict__ bucket, uint32_t *status,
                       uint32_t *ticket, int32_t *err) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     PassSmem &S = *reinterpret_cast<PassSmem *>(smem_raw);
@@ -151,7 +157,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
 #pragma unroll
     for (int i = 0; i < SORT_IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
-        const uint32_t d = pos < N ? ((k[i] >> shift) & (RADIX - 1)) : RADIX;   // RADIX = padding
+        const uint32_t d = pos < N ? ((k[i] >> shift) & mask) : RADIX;   // RADIX = padding
         const unsigned peers = __match_any_sync(FULL, d);
         const int leader = __ffs(peers) - 1;
         uint32_t base = 0;
@@ -165,7 +171,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     }
     __syncthreads();
 
-    // per digit (threads 0..255): tile count and exclusive prefix over warps,
+    // per digit (thread d < RADIX): tile count and exclusive prefix over warps,
     // then the look-back for the digit's prefix over earlier tiles
     const int d = tid;
     uint32_t sum = 0, x = 0;
@@ -229,7 +235,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     for (int i = 0; i < SORT_IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
         if (pos < N) {
-            const uint32_t d = (k[i] >> shift) & (RADIX - 1);
+            const uint32_t d = (k[i] >> shift) & mask;
             const uint32_t lp = S.local_off[d] + S.warp_cnt[warp][d] + rank[i];
             S.keys[lp] = k[i];
             S.vals[lp] = v[i];
@@ -241,7 +247,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     const int n = rem < SORT_TILE ? (int)rem : SORT_TILE;
     for (int j = tid; j < n; j += SORT_THREADS) {
         const uint32_t key = S.keys[j];
-        const uint32_t d = (key >> shift) & (RADIX - 1);
+        const uint32_t d = (key >> shift) & mask;
         const uint32_t gp = S.global_base[d] + (j - S.local_off[d]);
         if ((int64_t)gp < N) {   // always true unless a look-back gave up (flagged)
             keys_out[gp] = key;
@@ -260,6 +266,7 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
                        uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
                        bool *in_b) {
     const int passes = num_passes(key_bits);
+    const int bits = digit_bits(key_bits);
     *in_b = (passes & 1) != 0;
     if (N == 0 || passes == 0) {
         *in_b = false;
@@ -277,7 +284,7 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
     if (hist_grid > L.num_sms * 4) hist_grid = L.num_sms * 4;
     if (hist_grid < 1) hist_grid = 1;
     L.before("tbe_sort_histogram");
-    radix_hist_kernel<<<hist_grid, 256, 0, L.stream>>>(keys_a, N, passes, s.hist, s.status,
+    radix_hist_kernel<<<hist_grid, 256, 0, L.stream>>>(keys_a, N, passes, bits, s.hist, s.status,
                                                        zero_words);
     L.after();
     L.before("tbe_sort_buckets");
@@ -295,7 +302,7 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
     for (int ps = 0; ps < passes; ++ps) {
         L.before("tbe_sort_onesweep");
         radix_onesweep_kernel<<<(unsigned)s.ntiles, SORT_THREADS, smem, L.stream>>>(
-            ki, vi, ko, vo, N, ps * RADIX_BITS, s.hist + ps * RADIX,
+            ki, vi, ko, vo, N, ps * bits, (1u << bits) - 1, s.hist + ps * RADIX,
             s.status + (int64_t)ps * s.ntiles * RADIX, s.tickets + ps, status + 1);
         L.after();
         const uint32_t *tk = ko, *tv = vo;

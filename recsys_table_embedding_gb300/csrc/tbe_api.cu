@@ -400,7 +400,7 @@ int32_t tbe_version(void) { return 100; }
 
 namespace tbe {
 
-constexpr size_t STATIC_SCRATCH_BYTES = (size_t)4 * 1024 * 1024 + 8 * 1024;   // 4 MiB + 8 KiB
+constexpr size_t STATIC_SCRATCH_BYTES = (size_t)8 * 1024 * 1024 + 64 * 1024;  // 8 MiB + 64 KiB
 constexpr int64_t STATIC_SCRATCH_MAX_N = (int64_t)1 << 22;                    // 4,194,304 lookups
 constexpr int STATIC_MAX_DEVICES = 64;
 
