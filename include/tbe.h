@@ -81,7 +81,9 @@ typedef enum tbe_dtype { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
 /* Where runs with SL >= sl_threshold are reduced (FBTriton TBE redesign,
  * "Backward kernels", paths 2 and 3). */
 typedef enum tbe_long_run_mode {
-    TBE_LONG_AUTO = 0,       /* = TBE_LONG_FUSED on this GPU */
+    TBE_LONG_AUTO = 0,       /* = TBE_LONG_TWO_KERNEL: on GB300 the fused launch's per-chunk
+                                fence and arrival round trip queue behind the gather's
+                                DRAM misses and cost more than the extra launch */
     TBE_LONG_TWO_KERNEL = 1, /* grad_accum into the workspace + a separate apply kernel */
     TBE_LONG_FUSED = 2       /* one launch; the last-arriving chunk applies the update */
 } tbe_long_run_mode;
@@ -167,6 +169,9 @@ typedef struct tbe_meta {
     int32_t *long_chunk_base;           /* [max_long] first chunk slot of long run l */
     int32_t *chunk_owner;               /* [max_chunks] long run of chunk slot c */
     int32_t *arrive;                    /* [max_long] arrival counters of the fused long-run path */
+    int32_t *chunk_desc;                /* [max_chunks][8] per chunk slot: first and end sorted
+                                           position, key, table, long run, first slot of the run,
+                                           chunks of the run, 0 */
     uint16_t *hist;
     size_t bytes;
 } tbe_meta;

@@ -43,6 +43,7 @@ struct BwdParams {
     const int32_t *long_run;
     const int32_t *long_chunk_base;
     const int32_t *chunk_owner;
+    const int32_t *chunk_desc;
     void *partials;
     int32_t *arrive;
     int32_t *status;
@@ -161,8 +162,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 // mbarrier completes when all its bytes have landed.  Lanes then read their
 // own 16-byte vectors of each row from shared memory.
 
-constexpr int STAGES = 3;
+#ifndef TBE_BWD_STAGES
+#define TBE_BWD_STAGES 3
+#endif
+#ifndef TBE_CHUNK_THREADS
+#define TBE_CHUNK_THREADS 128
+#endif
+constexpr int STAGES = TBE_BWD_STAGES;
 constexpr int STAGE_BYTES = 4096;
+constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;   // 4 warps: three blocks fit an SM at chunk 256
+constexpr int PV = 8;                // payloads a lane prefetches in registers
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -181,116 +190,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 // shared memory of one warp: STAGES x STAGE_BYTES ring, STAGES mbarriers,
-// then the element offset and weight of each lookup of the range
+// then two buffers (current and next chunk) of the element offset and the
+// weight of each lookup
 __host__ __device__ constexpr int warp_smem_bytes(int chunk) {
-    return (STAGES * STAGE_BYTES + 64 + chunk * 8 + 127) / 128 * 128;
+    return (STAGES * STAGE_BYTES + 64 + 2 * chunk * 8 + 127) / 128 * 128;
 }
 
-struct WarpRing {
-    unsigned char *ring;
-    uint32_t bar0;        // shared address of the first mbarrier
-    uint32_t *off;        // element offset of each lookup's gradient row from G_t
-    float *w;
-    uint32_t phase;       // bit s = parity of stage s's next completion
+// One chunk of a long run, as the route kernel describes it.
+struct Chunk {
+    int32_t s, e;      // sorted positions [s, e)
+    uint32_t key;
+    int t, l, cb, nch; // table, long run, its first chunk slot and chunk count
 };
 
-__device__ __forceinline__ WarpRing warp_ring(unsigned char *wsm, int chunk, int lane) {
-    WarpRing r;
-    r.ring = wsm;
-    r.bar0 = smem_addr(wsm + STAGES * STAGE_BYTES);
-    r.off = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);
-    r.w = reinterpret_cast<float *>(r.off + chunk);
-    r.phase = 0;
-    if (lane == 0)
-        for (int i = 0; i < STAGES; ++i) bar_init(r.bar0 + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncwarp();
-    return r;
+__device__ __forceinline__ Chunk load_chunk(const int32_t *desc, int ci) {
+    const int4 a = __ldg(reinterpret_cast<const int4 *>(desc) + 2 * (int64_t)ci);
+    const int4 b = __ldg(reinterpret_cast<const int4 *>(desc) + 2 * (int64_t)ci + 1);
+    Chunk c;
+    c.s = a.x; c.e = a.y; c.key = (uint32_t)a.z; c.t = a.w;
+    c.l = b.x; c.cb = b.y; c.nch = b.z;
+    return c;
 }
-
-// Sum w_p * G[b(p), t*D + d] over sorted positions [s, e) (at most `chunk`)
-// into acc (per lane: elements li*4 + q*LPR*4 .. +4), then combine the 32/LPR
-// sub-groups.  Returns false if a copy wait gave up (bounded).
-template <typename ACC, int LPR, int NV>
-__device__ __forceinline__ bool gather_rows(ACC (&acc)[NV][4], const BwdParams &p, int t, bool wt,
-                                            int32_t s, int32_t e, int lane, int sub, int li,
-                                            WarpRing &rg) {
-    constexpr int RPI = 32 / LPR;
-    const uint32_t row_bytes = (uint32_t)p.D * 4;
-    const int R = STAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
-    const float *Gt = p.G + (int64_t)t * p.D;
-    const int64_t rowstride = (int64_t)p.T * p.D;
-    const int64_t tB = (int64_t)t * p.B;
-#pragma unroll
-    for (int q = 0; q < NV; ++q)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
-    const int n = e - s;
-    __syncwarp();   // the previous range's readers are done with off/w
-    for (int i = lane; i < n; i += 32) {
-        const uint32_t v = __ldg(p.vals + s + i);
-        int b;
-        float w = 1.f;
-        if (p.payload_pos) {
-            b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
-            if (wt) w = __ldg(p.psw + v);
-        } else {
-            b = (int)v;
-        }
-        // only malformed (overlapping) offsets can give a bag outside the
-        // run's table: such a lookup copies row 0 with weight 0
-        const bool ok = b >= 0 && (int64_t)b < p.B;
-        rg.off[i] = ok ? (uint32_t)((int64_t)b * rowstride) : 0u;
-        rg.w[i] = ok ? w : 0.f;
-    }
-    __syncwarp();
-    const int nst = (n + R - 1) / R;
-    auto produce = [&](int k) {
-        const int st = k % STAGES;
-        const int rows = min(R, n - k * R);
-        const uint32_t bar = rg.bar0 + 8 * st;
-        if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
-        __syncwarp();
-        const uint32_t dst0 = smem_addr(rg.ring + st * STAGE_BYTES);
-        for (int j = lane; j < rows; j += 32)
-            bulk_g2s(dst0 + j * row_bytes, Gt + rg.off[k * R + j], row_bytes, bar);
-    };
-    for (int k = 0; k < nst && k < STAGES; ++k) produce(k);
-    bool ok = true;
-    for (int k = 0; k < nst; ++k) {
-        const int st = k % STAGES;
-        const uint32_t bar = rg.bar0 + 8 * st;
-        const uint32_t par = (rg.phase >> st) & 1u;
-        if (!mbar_wait_bounded(bar, par)) {
-            // stop issuing: give the copies still in flight (stages k+1 ..
-            // k+STAGES-1 of this range) one more bounded wait before the
-            // caller flags the failure and ends the warp's work
-            for (int k2 = k + 1; k2 < nst && k2 < k + STAGES; ++k2)
-                mbar_wait_bounded(rg.bar0 + 8 * (k2 % STAGES), (rg.phase >> (k2 % STAGES)) & 1u);
-            ok = false;
-            break;
-        }
-        rg.phase ^= 1u << st;
-        const int rows = min(R, n - k * R);
-        const unsigned char *stage = rg.ring + st * STAGE_BYTES;
-        for (int j = sub; j < rows; j += RPI) {
-            const float w = rg.w[k * R + j];
-            const float4 *src = reinterpret_cast<const float4 *>(stage + j * row_bytes) + li;
-#pragma unroll
-            for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * LPR], w);
-        }
-        __syncwarp();   // everyone is done reading the stage before it is refilled
-        if (k + STAGES < nst) produce(k + STAGES);
-    }
-#pragma unroll
-    for (int sh = LPR; sh < 32; sh <<= 1)
-#pragma unroll
-        for (int q = 0; q < NV; ++q)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
-    return __all_sync(FULL, ok);
-}
-
 // Exact rowwise Adagrad on row `row` from the reduced gradient in acc:
 //   m += mean_d(g^2);  w -= lr * g / (sqrt(m) + eps)
 // Only lanes of sub-group 0 hold meaningful values; every lane takes part in
@@ -459,41 +379,174 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
     }
 }
 
+// Long-run chunks.  A warp takes chunk slots ci, ci + nwarps, ... and treats
+// their gradient rows as one stream of ring stages: while it reduces chunk j,
+// the ring already holds copies of chunk j+1, whose lookups were staged in
+// the second buffer, so neither the chunk's metadata, its payload loads nor
+// the fused tail leave the copy engine idle.  A stage never spans two
+// chunks.  The partial of chunk slot ci is the sum over its range in sorted
+// order, so results do not depend on which warp took which chunk.
 template <typename WT, int LPR, int NV, bool FUSED>
-__global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int RPI = 32 / LPR;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nchunks = p.counters[C_NUM_CHUNKS];
-    WarpRing rg = warp_ring(smem_raw + (threadIdx.x >> 5) * warp_smem_bytes(p.chunk), p.chunk, lane);
-    for (int ci = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; ci < nchunks; ci += nwarps) {
-        const int l = __ldg(p.chunk_owner + ci);
-        const int r = __ldg(p.long_run + l);
-        const int cb = __ldg(p.long_chunk_base + l);
-        const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
-        const int32_t s = rs + (ci - cb) * p.chunk;
-        const int32_t e = min(s + p.chunk, re);
-        const int64_t key = __ldg(p.unique_keys + r);
-        const int t = table_of_key(p.table_offset, p.T, key);
-        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
-        ACC acc[NV][4];
-        if (!gather_rows<ACC, LPR, NV>(acc, p, t, wt, s, e, lane, sub, li, rg)) {
-            if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
-            return;   // results are invalid (flagged); issue nothing more
+    int ci = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (ci >= nchunks) return;
+
+    unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * warp_smem_bytes(p.chunk);
+    const uint32_t ring0 = smem_addr(wsm);
+    const uint32_t bar0 = smem_addr(wsm + STAGES * STAGE_BYTES);
+    uint32_t *offb = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);  // [2][chunk]
+    float *wgt = reinterpret_cast<float *>(offb + 2 * p.chunk);                       // [2][chunk]
+    if (lane == 0)
+        for (int i = 0; i < STAGES; ++i) bar_init(bar0 + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    const uint32_t row_bytes = (uint32_t)p.D * 4;
+    const int R = STAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
+    const int64_t rowstride = (int64_t)p.T * p.D;
+
+    // payload of lookups [s, s + PV*32) into registers (issued early)
+    uint32_t pv[PV];
+    auto fetch = [&](const Chunk &c) {
+#pragma unroll
+        for (int k = 0; k < PV; ++k) {
+            const int32_t i = c.s + lane + 32 * k;
+            pv[k] = i < c.e ? __ldg(p.vals + i) : 0u;
         }
+    };
+    // element offset (from G_t) and weight of each lookup of c into buffer buf
+    auto stage = [&](const Chunk &c, int buf) {
+        const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + c.t) != 0);
+        const int64_t tB = (int64_t)c.t * p.B;
+        const int n = c.e - c.s;
+        uint32_t *o = offb + buf * p.chunk;
+        float *w = wgt + buf * p.chunk;
+        auto put = [&](int i, uint32_t v) {
+            int b;
+            float x = 1.f;
+            if (p.payload_pos) {
+                b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
+                if (wt) x = __ldg(p.psw + v);
+            } else {
+                b = (int)v;
+            }
+            // only malformed (overlapping) offsets can give a bag outside the
+            // run's table: such a lookup copies row 0 with weight 0
+            const bool ok = b >= 0 && (int64_t)b < p.B;
+            o[i] = ok ? (uint32_t)((int64_t)b * rowstride) : 0u;
+            w[i] = ok ? x : 0.f;
+        };
+#pragma unroll
+        for (int k = 0; k < PV; ++k)
+            if (lane + 32 * k < n) put(lane + 32 * k, pv[k]);
+        for (int i = lane + 32 * PV; i < n; i += 32) put(i, __ldg(p.vals + c.s + i));
+        __syncwarp();
+    };
+
+    uint32_t gprod = 0, gcons = 0, phase = 0;
+    auto produce = [&](const Chunk &c, int buf, int k) {
+        const int st = (int)(gprod % STAGES);
+        const int rows = min(R, c.e - c.s - k * R);
+        const uint32_t bar = bar0 + 8 * st;
+        if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
+        __syncwarp();
+        const float *Gt = p.G + (int64_t)c.t * p.D;
+        const uint32_t *o = offb + buf * p.chunk + k * R;
+        const uint32_t dst0 = ring0 + st * STAGE_BYTES;
+        for (int j = lane; j < rows; j += 32) bulk_g2s(dst0 + j * row_bytes, Gt + o[j], row_bytes, bar);
+        ++gprod;
+    };
+
+    Chunk cur = load_chunk(p.chunk_desc, ci);
+    fetch(cur);
+    stage(cur, 0);
+    int buf = 0;
+    int ni = ci + nwarps;
+    bool has_next = ni < nchunks;
+    Chunk nxt = cur;
+    if (has_next) nxt = load_chunk(p.chunk_desc, ni);
+    int cur_nst = (cur.e - cur.s + R - 1) / R;
+    int pk = 0;              // next stage to issue of the chunk being issued
+    bool p_next = false;     // issuing into nxt already
+    bool next_staged = false;
+    auto refill = [&]() {
+        while (gprod - gcons < (uint32_t)STAGES) {
+            if (!p_next) {
+                if (pk < cur_nst) { produce(cur, buf, pk++); continue; }
+                if (!has_next || !next_staged) break;
+                p_next = true;
+                pk = 0;
+            }
+            if (pk < (nxt.e - nxt.s + R - 1) / R) produce(nxt, buf ^ 1, pk++);
+            else break;
+        }
+    };
+    refill();
+
+    for (;;) {
+        next_staged = false;
+        if (has_next) fetch(nxt);   // latency overlaps the first stage below
+        ACC acc[NV][4];
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+        const float *w = wgt + buf * p.chunk;
+        for (int k = 0; k < cur_nst; ++k) {
+            const int st = (int)(gcons % STAGES);
+            if (!mbar_wait_bounded(bar0 + 8 * st, (phase >> st) & 1u)) {
+                // stop issuing: give the copies still in flight one more
+                // bounded wait each, flag the failure, end the warp's work
+                for (uint32_t g = gcons + 1; g < gprod; ++g)
+                    mbar_wait_bounded(bar0 + 8 * (g % STAGES), (phase >> (g % STAGES)) & 1u);
+                if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
+                return;
+            }
+            phase ^= 1u << st;
+            const int rows = min(R, cur.e - cur.s - k * R);
+            const unsigned char *sp = wsm + st * STAGE_BYTES;
+            for (int j = sub; j < rows; j += RPI) {
+                const float x = w[k * R + j];
+                const float4 *src = reinterpret_cast<const float4 *>(sp + j * row_bytes) + li;
+#pragma unroll
+                for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * LPR], x);
+            }
+            ++gcons;
+            __syncwarp();   // the stage is read before it is refilled
+            if (!next_staged && has_next) {
+                stage(nxt, buf ^ 1);
+                next_staged = true;
+            }
+            refill();
+        }
+        if (!next_staged && has_next) {
+            stage(nxt, buf ^ 1);
+            next_staged = true;
+            refill();
+        }
+#pragma unroll
+        for (int sh = LPR; sh < 32; sh <<= 1)
+#pragma unroll
+            for (int q = 0; q < NV; ++q)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
         ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
         if (sub == 0)
 #pragma unroll
             for (int q = 0; q < NV; ++q) st_part(part + q * LPR * 4, acc[q]);
         if constexpr (FUSED) {
-            const int nch = (re - rs + p.chunk - 1) / p.chunk;
             __threadfence();
             __syncwarp();
             int old = 0;
-            if (lane == 0) old = atomicAdd(p.arrive + l, 1);
+            if (lane == 0) old = atomicAdd(p.arrive + cur.l, 1);
             old = __shfl_sync(FULL, old, 0);
-            if (old == nch - 1) {
+            if (old == cur.nch - 1) {
                 __threadfence();
 #pragma unroll
                 for (int q = 0; q < NV; ++q)
@@ -501,11 +554,24 @@ __global__ void __launch_bounds__(256) tbe_bwd_chunk_kernel(const BwdParams p) {
                     for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
                 if (sub == 0)
                     sum_partials<true, ACC, LPR, NV>(acc, reinterpret_cast<const ACC *>(p.partials),
-                                                    cb, nch, p.D, li);
-                adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
-                if (lane == 0) p.arrive[l] = 0;
+                                                    cur.cb, cur.nch, p.D, li);
+                adagrad_apply<WT, ACC, LPR, NV>(acc, p, (int64_t)cur.key, lane, sub, li);
+                if (lane == 0) p.arrive[cur.l] = 0;
             }
         }
+        if (!has_next) break;
+        // the next chunk becomes current; stages already issued for it stay
+        ci = ni;
+        cur = nxt;
+        buf ^= 1;
+        cur_nst = (cur.e - cur.s + R - 1) / R;
+        if (!p_next) pk = 0;
+        p_next = false;
+        ni += nwarps;
+        has_next = ni < nchunks;
+        if (has_next) nxt = load_chunk(p.chunk_desc, ni);
+        next_staged = false;
+        refill();
     }
 }
 
@@ -541,9 +607,9 @@ size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype) {
 }
 
 template <typename K>
-static int persistent_grid(K kernel, int num_sms, size_t smem = 0) {
+static int persistent_grid(K kernel, int num_sms, size_t smem = 0, int threads = 256) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (per_sm < 1) per_sm = 1;
     return num_sms * per_sm;
 }
@@ -558,14 +624,14 @@ static constexpr int short_vectors_per_lane(int V) {
 
 template <typename WT, int LPR, int NV>
 static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
-    const size_t csm = (size_t)8 * warp_smem_bytes(p.chunk);
+    const size_t csm = (size_t)(CHUNK_THREADS / 32) * warp_smem_bytes(p.chunk);
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, false>;
         cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
         cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
         L.before("tbe_bwd_grad_accum");
-        kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
+        kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     } else {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, true>;
@@ -573,7 +639,7 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
         L.before("tbe_bwd_fused_long");
-        kc<<<persistent_grid(kc, L.num_sms, csm), 256, csm, L.stream>>>(p);
+        kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     }
     // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
@@ -627,6 +693,7 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.long_run = m->long_run;
     p.long_chunk_base = m->long_chunk_base;
     p.chunk_owner = m->chunk_owner;
+    p.chunk_desc = m->chunk_desc;
     p.partials = a.partials;
     p.arrive = a.arrive;
     p.status = a.status;

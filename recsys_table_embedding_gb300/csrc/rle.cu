@@ -119,22 +119,36 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
 // Long runs (SL >= sl_threshold) get a slot l and ceil(SL/chunk) chunk slots.
 // The order of slots depends on atomic arrival; results do not (each chunk
 // covers a fixed position range and partials are summed in chunk order).
+// Each chunk slot also gets a descriptor -- its position range, key, table,
+// long run, the run's first slot and chunk count -- so the long-run kernel
+// reads one 32-byte record per chunk instead of chasing the run tables.
 __global__ void __launch_bounds__(256) route_kernel(const int32_t *__restrict__ seg_off,
-                                                    int32_t *counters, int32_t *long_run,
+                                                    const uint32_t *__restrict__ unique_keys,
+                                                    const int64_t *__restrict__ table_offset,
+                                                    int T, int32_t *counters, int32_t *long_run,
                                                     int32_t *long_chunk_base,
-                                                    int32_t *chunk_owner, int32_t *arrive,
-                                                    int sl_threshold, int chunk) {
+                                                    int32_t *chunk_owner, int32_t *chunk_desc,
+                                                    int32_t *arrive, int sl_threshold, int chunk) {
     const int U = counters[C_NUM_UNIQUE];
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < U; r += gridDim.x * blockDim.x) {
-        const int len = seg_off[r + 1] - seg_off[r];
+        const int32_t rs = seg_off[r], re = seg_off[r + 1];
+        const int len = re - rs;
         if (len < sl_threshold) continue;
         const int nch = (len + chunk - 1) / chunk;
         const int l = atomicAdd(counters + C_NUM_LONG, 1);
         const int cb = atomicAdd(counters + C_NUM_CHUNKS, nch);
+        const uint32_t key = unique_keys[r];
+        const int t = table_of_key(table_offset, T, key);
         long_run[l] = r;
         long_chunk_base[l] = cb;
         arrive[l] = 0;
-        for (int c = 0; c < nch; ++c) chunk_owner[cb + c] = l;
+        for (int c = 0; c < nch; ++c) {
+            chunk_owner[cb + c] = l;
+            const int32_t s = rs + c * chunk;
+            int4 *d = reinterpret_cast<int4 *>(chunk_desc + (int64_t)(cb + c) * 8);
+            d[0] = make_int4(s, min(s + chunk, re), (int)key, t);
+            d[1] = make_int4(l, cb, nch, 0);
+        }
     }
 }
 
@@ -147,7 +161,8 @@ __global__ void zero_first_kernel(int32_t *p) { p[0] = 0; }
 tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_t sentinel,
                       uint32_t *unique_keys, int32_t *seg_off, int32_t *counters,
                       int32_t *long_run, int32_t *long_chunk_base, int32_t *chunk_owner,
-                      int32_t *arrive, int sl_threshold, int chunk, void *ws) {
+                      int32_t *chunk_desc, int32_t *arrive, const int64_t *table_offset, int T,
+                      int sl_threshold, int chunk, void *ws) {
     L.before("tbe_rle_zero");
     zero_counters_kernel<<<1, 32, 0, L.stream>>>(counters);
     L.after();
@@ -174,8 +189,9 @@ tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_
     int grid = (int)((N + 255) / 256);
     if (grid > L.num_sms * 8) grid = L.num_sms * 8;
     L.before("tbe_route");
-    route_kernel<<<grid, 256, 0, L.stream>>>(seg_off, counters, long_run, long_chunk_base,
-                                             chunk_owner, arrive, sl_threshold, chunk);
+    route_kernel<<<grid, 256, 0, L.stream>>>(seg_off, unique_keys, table_offset, T, counters,
+                                             long_run, long_chunk_base, chunk_owner, chunk_desc,
+                                             arrive, sl_threshold, chunk);
     L.after();
     return TBE_OK;
 }

@@ -101,7 +101,7 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     pr->payload_pos = bt->per_sample_weights != nullptr ? 1 : 0;
     pr->sl_threshold = c.sl_threshold;
     pr->chunk = c.chunk;
-    pr->long_mode = c.long_run_mode == TBE_LONG_TWO_KERNEL ? TBE_LONG_TWO_KERNEL : TBE_LONG_FUSED;
+    pr->long_mode = c.long_run_mode == TBE_LONG_FUSED ? TBE_LONG_FUSED : TBE_LONG_TWO_KERNEL;
     pr->max_long = bt->N / c.sl_threshold + 1;
     pr->max_chunks = bt->N / c.chunk + pr->max_long + 1;
     pr->path = 1;
@@ -123,7 +123,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Meta layout (each array 256-byte aligned).
 struct MetaLayout {
     size_t keys_a, vals_a, keys_b, vals_b, bag_of, unique_keys, seg_off, counters, long_run,
-        long_chunk_base, arrive, chunk_owner, hist, total;
+        long_chunk_base, arrive, chunk_owner, chunk_desc, hist, total;
 };
 
 static MetaLayout meta_layout(const Problem &pr) {
@@ -149,10 +149,11 @@ static MetaLayout meta_layout(const Problem &pr) {
         m.long_chunk_base = take((size_t)pr.max_long * 4);
         m.arrive = take((size_t)pr.max_long * 4);
         m.chunk_owner = take((size_t)pr.max_chunks * 4);
+        m.chunk_desc = take((size_t)pr.max_chunks * 32);
         m.hist = (size_t)-1;
     } else {
         m.keys_a = m.vals_a = m.keys_b = m.vals_b = m.bag_of = m.unique_keys = m.seg_off =
-            m.long_run = m.long_chunk_base = m.arrive = m.chunk_owner = (size_t)-1;
+            m.long_run = m.long_chunk_base = m.arrive = m.chunk_owner = m.chunk_desc = (size_t)-1;
         m.counters = take(C_COUNT * 4);
         m.hist = take((size_t)pr.NB * 64 * 2);
     }
@@ -205,7 +206,8 @@ static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batc
     meta->sorted_vals = in_b ? meta->vals_b : meta->vals_a;
     return launch_rle(L, meta->sorted_keys, pr.N, (uint32_t)pr.rows_total, meta->unique_keys,
                       meta->seg_off, meta->counters, meta->long_run, meta->long_chunk_base,
-                      meta->chunk_owner, meta->arrive, pr.sl_threshold, pr.chunk, ws);
+                      meta->chunk_owner, meta->chunk_desc, meta->arrive, tab->table_offset,
+                      tab->T, pr.sl_threshold, pr.chunk, ws);
 }
 
 }  // namespace tbe
@@ -271,6 +273,7 @@ tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes, const t
     meta->long_run = (int32_t *)at(L.long_run);
     meta->long_chunk_base = (int32_t *)at(L.long_chunk_base);
     meta->chunk_owner = (int32_t *)at(L.chunk_owner);
+    meta->chunk_desc = (int32_t *)at(L.chunk_desc);
     meta->hist = (uint16_t *)at(L.hist);
     meta->bytes = L.total;
     meta->arrive = (int32_t *)at(L.arrive);

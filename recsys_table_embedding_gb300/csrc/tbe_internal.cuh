@@ -141,7 +141,8 @@ size_t rle_workspace_bytes(int64_t N);
 tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_t sentinel,
                       uint32_t *unique_keys, int32_t *seg_off, int32_t *counters,
                       int32_t *long_run, int32_t *long_chunk_base, int32_t *chunk_owner,
-                      int32_t *arrive, int sl_threshold, int chunk, void *ws);
+                      int32_t *chunk_desc, int32_t *arrive, const int64_t *table_offset, int T,
+                      int sl_threshold, int chunk, void *ws);
 
 // --- backward.cu
 struct BwdArgs {
