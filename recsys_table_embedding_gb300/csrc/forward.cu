@@ -97,18 +97,26 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     return v;
 }
 
+// The kernel is issue-bound (most row reads hit L2), so the inner loop is
+// kept short: full steps of 32/LPR*U rows whose lookups are all in range run
+// without predicates or branches; the rest of a 32-lookup block (and any
+// block with an out-of-range index) goes one 32/LPR-row step at a time with
+// per-row checks.  (t, b) of the next bag are stepped, not divided.
 template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED>
 __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     constexpr int VEC = VB / (int)sizeof(WT);   // elements per lane vector
     constexpr int RPI = 32 / LPR;
+    constexpr int STEP = RPI * U;               // rows of a full step
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    int t = (int)(bag / p.B);
+    int64_t b = bag - (int64_t)t * p.B;
+    const int tstep = (int)(nwarps / p.B);
+    const int64_t bstep = nwarps - (int64_t)tstep * p.B;
     int oob = 0;
-    for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < p.NB;
-         bag += nwarps) {
-        const int t = (int)(bag / p.B);
-        const int64_t b = bag - (int64_t)t * p.B;
+    for (; bag < p.NB; bag += nwarps) {
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
         int32_t start = __ldg(p.offsets + bag);
@@ -141,28 +149,40 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
                 if (p.bag_of != nullptr) p.bag_of[base + lane] = (int32_t)bag;
             }
             const unsigned vmask = __ballot_sync(FULL, valid);
-            for (int j = 0; j < n; j += RPI * U) {
-                Vec<VB> v[U][NV];
-                float wv[U];
-                bool ok[U];
+            // full steps while every lookup of the block is in range
+            int j = 0;
+            if (vmask == (n == 32 ? FULL : ((1u << n) - 1u))) {
+                for (; j + STEP <= n; j += STEP) {
+                    Vec<VB> v[U][NV];
+                    float wv[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int k = j + u * RPI + sub;
-                    const int src = k & 31;
-                    const int32_t ik = __shfl_sync(FULL, idx, src);
-                    wv[u] = WEIGHTED ? __shfl_sync(FULL, w, src) : 1.f;
-                    ok[u] = k < n && ((vmask >> src) & 1u);
-                    if (ok[u]) {
+                    for (int u = 0; u < U; ++u) {
+                        const int32_t ik = __shfl_sync(FULL, idx, j + u * RPI + sub);
+                        wv[u] = WEIGHTED ? __shfl_sync(FULL, w, j + u * RPI + sub) : 1.f;
                         const WT *r = Wt + (int64_t)ik * p.D;
 #pragma unroll
                         for (int q = 0; q < NV; ++q) v[u][q] = ldg_vec<VB>(r + q * LPR * VEC);
                     }
-                }
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (ok[u])
+                    for (int u = 0; u < U; ++u)
 #pragma unroll
                         for (int q = 0; q < NV; ++q) accum<WT, VB>(acc[q], v[u][q], wv[u]);
+                }
+            }
+            // the rest, one 32/LPR-row step at a time
+            for (; j < n; j += RPI) {
+                const int k = j + sub;
+                const int src = k & 31;
+                const int32_t ik = __shfl_sync(FULL, idx, src);
+                const float wk = WEIGHTED ? __shfl_sync(FULL, w, src) : 1.f;
+                if (k < n && ((vmask >> src) & 1u)) {
+                    const WT *r = Wt + (int64_t)ik * p.D;
+                    Vec<VB> v[NV];
+#pragma unroll
+                    for (int q = 0; q < NV; ++q) v[q] = ldg_vec<VB>(r + q * LPR * VEC);
+#pragma unroll
+                    for (int q = 0; q < NV; ++q) accum<WT, VB>(acc[q], v[q], wk);
+                }
             }
         }
 #pragma unroll
@@ -175,6 +195,12 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
             float *o = p.out + (b * p.T + t) * (int64_t)p.D + li * VEC;
 #pragma unroll
             for (int q = 0; q < NV; ++q) store_out<VEC>(o + q * LPR * VEC, acc[q]);
+        }
+        t += tstep;
+        b += bstep;
+        if (b >= p.B) {
+            b -= p.B;
+            ++t;
         }
     }
     oob = warp_sum_i(oob);
@@ -240,7 +266,7 @@ static int grid_for(K kernel, int threads, int64_t work_warps, int num_sms) {
 }
 
 #ifndef TBE_FWD_ROWS
-#define TBE_FWD_ROWS 4   // weight rows in flight per warp (4, 8, 16 measured; 4 best)
+#define TBE_FWD_ROWS 8   // weight rows of a full step per warp
 #endif
 
 template <typename WT, int VB, int LPR, int NV>
