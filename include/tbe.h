@@ -167,11 +167,14 @@ typedef struct tbe_meta {
     int32_t *counters;
     int32_t *long_run;                  /* [max_long] run id of long run l */
     int32_t *long_chunk_base;           /* [max_long] first chunk slot of long run l */
-    int32_t *chunk_owner;               /* [max_chunks] long run of chunk slot c */
+    int32_t *chunk_order;               /* [max_chunks] chunk slot taken c-th by the long-run
+                                           kernel: slots grouped by table and batch window of
+                                           their first lookup's bag (batches of B >= 4096); scratch
+                                           for smaller batches, whose slot c is taken c-th */
     int32_t *arrive;                    /* [max_long] arrival counters of the fused long-run path */
     int32_t *chunk_desc;                /* [max_chunks][8] per chunk slot: first and end sorted
                                            position, key, table, long run, first slot of the run,
-                                           chunks of the run, 0 */
+                                           chunks of the run, window key */
     uint16_t *hist;
     size_t bytes;
 } tbe_meta;

@@ -42,7 +42,7 @@ struct BwdParams {
     const int32_t *counters;
     const int32_t *long_run;
     const int32_t *long_chunk_base;
-    const int32_t *chunk_owner;
+    const int32_t *chunk_order;   // null: slot c is taken c-th
     const int32_t *chunk_desc;
     void *partials;
     int32_t *arrive;
@@ -201,14 +201,18 @@ struct Chunk {
     int32_t s, e;      // sorted positions [s, e)
     uint32_t key;
     int t, l, cb, nch; // table, long run, its first chunk slot and chunk count
+    int slot;          // chunk slot (index of its descriptor and its partial)
 };
 
-__device__ __forceinline__ Chunk load_chunk(const int32_t *desc, int ci) {
-    const int4 a = __ldg(reinterpret_cast<const int4 *>(desc) + 2 * (int64_t)ci);
-    const int4 b = __ldg(reinterpret_cast<const int4 *>(desc) + 2 * (int64_t)ci + 1);
+// the chunk taken ci-th: slot chunk_order[ci], or ci without an order
+__device__ __forceinline__ Chunk load_chunk(const BwdParams &p, int ci) {
+    const int slot = p.chunk_order != nullptr ? __ldg(p.chunk_order + ci) : ci;
+    const int4 a = __ldg(reinterpret_cast<const int4 *>(p.chunk_desc) + 2 * (int64_t)slot);
+    const int4 b = __ldg(reinterpret_cast<const int4 *>(p.chunk_desc) + 2 * (int64_t)slot + 1);
     Chunk c;
     c.s = a.x; c.e = a.y; c.key = (uint32_t)a.z; c.t = a.w;
     c.l = b.x; c.cb = b.y; c.nch = b.z;
+    c.slot = slot;
     return c;
 }
 // Exact rowwise Adagrad on row `row` from the reduced gradient in acc:
@@ -379,13 +383,16 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
     }
 }
 
-// Long-run chunks.  A warp takes chunk slots ci, ci + nwarps, ... and treats
-// their gradient rows as one stream of ring stages: while it reduces chunk j,
-// the ring already holds copies of chunk j+1, whose lookups were staged in
-// the second buffer, so neither the chunk's metadata, its payload loads nor
-// the fused tail leave the copy engine idle.  A stage never spans two
-// chunks.  The partial of chunk slot ci is the sum over its range in sorted
-// order, so results do not depend on which warp took which chunk.
+// Long-run chunks.  A warp takes the chunks at order positions ci,
+// ci + nwarps, ... (slot chunk_order[ci]: slots grouped by the batch window
+// of their first bag, so warps working at the same time read gradient rows
+// of nearby bags, which L2 then serves) and treats their gradient rows as one
+// stream of ring stages: while it reduces chunk j, the ring already holds
+// copies of chunk j+1, whose lookups were staged in the second buffer, so
+// neither the chunk's metadata, its payload loads nor the fused tail leave
+// the copy engine idle.  A stage never spans two chunks.  The partial of a
+// chunk slot is the sum over its range in sorted order, so results do not
+// depend on the order or on which warp took which chunk.
 template <typename WT, int LPR, int NV, bool FUSED>
 __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
@@ -463,14 +470,14 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         ++gprod;
     };
 
-    Chunk cur = load_chunk(p.chunk_desc, ci);
+    Chunk cur = load_chunk(p, ci);
     fetch(cur);
     stage(cur, 0);
     int buf = 0;
     int ni = ci + nwarps;
     bool has_next = ni < nchunks;
     Chunk nxt = cur;
-    if (has_next) nxt = load_chunk(p.chunk_desc, ni);
+    if (has_next) nxt = load_chunk(p, ni);
     int cur_nst = (cur.e - cur.s + R - 1) / R;
     int pk = 0;              // next stage to issue of the chunk being issued
     bool p_next = false;     // issuing into nxt already
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             for (int q = 0; q < NV; ++q)
 #pragma unroll
                 for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
-        ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)ci * p.D + li * 4;
+        ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)cur.slot * p.D + li * 4;
         if (sub == 0)
 #pragma unroll
             for (int q = 0; q < NV; ++q) st_part(part + q * LPR * 4, acc[q]);
@@ -561,7 +568,6 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         }
         if (!has_next) break;
         // the next chunk becomes current; stages already issued for it stay
-        ci = ni;
         cur = nxt;
         buf ^= 1;
         cur_nst = (cur.e - cur.s + R - 1) / R;
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         p_next = false;
         ni += nwarps;
         has_next = ni < nchunks;
-        if (has_next) nxt = load_chunk(p.chunk_desc, ni);
+        if (has_next) nxt = load_chunk(p, ni);
         next_staged = false;
         refill();
     }
@@ -692,7 +698,7 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.counters = m->counters;
     p.long_run = m->long_run;
     p.long_chunk_base = m->long_chunk_base;
-    p.chunk_owner = m->chunk_owner;
+    p.chunk_order = chunk_order_on(a.bt->B) ? m->chunk_order : nullptr;
     p.chunk_desc = m->chunk_desc;
     p.partials = a.partials;
     p.arrive = a.arrive;

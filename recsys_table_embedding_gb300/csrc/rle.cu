@@ -18,9 +18,19 @@ constexpr int RLE_THREADS = 256;
 constexpr int RLE_IPT = 16;
 constexpr int RLE_TILE = RLE_THREADS * RLE_IPT;
 
+// tile head counts, then CHUNK_WINDOWS_MAX window counters
 size_t rle_workspace_bytes(int64_t N) {
     const int64_t ntiles = (N + RLE_TILE - 1) / RLE_TILE;
-    return (size_t)(ntiles + 1) * 4 + 256;
+    return ((size_t)(ntiles + 1) * 4 + 255) / 256 * 256 + (size_t)CHUNK_WINDOWS_MAX * 4;
+}
+
+bool chunk_order_on(int64_t B) { return B >= CHUNK_ORDER_MIN_B; }
+
+// windows of 2^shift bags (at least 512) with T * windows <= CHUNK_WINDOWS_MAX
+int chunk_window_shift(int64_t B, int T) {
+    int s = 9;
+    while ((int64_t)T * ((B + (int64_t(1) << s) - 1) >> s) > CHUNK_WINDOWS_MAX) ++s;
+    return s;
 }
 
 __device__ __forceinline__ int block_excl_scan(int x, int *tot_smem, int &total) {
@@ -119,37 +129,118 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
 // Long runs (SL >= sl_threshold) get a slot l and ceil(SL/chunk) chunk slots.
 // The order of slots depends on atomic arrival; results do not (each chunk
 // covers a fixed position range and partials are summed in chunk order).
-// Each chunk slot also gets a descriptor -- its position range, key, table,
-// long run, the run's first slot and chunk count -- so the long-run kernel
-// reads one 32-byte record per chunk instead of chasing the run tables.
-__global__ void __launch_bounds__(256) route_kernel(const int32_t *__restrict__ seg_off,
-                                                    const uint32_t *__restrict__ unique_keys,
-                                                    const int64_t *__restrict__ table_offset,
-                                                    int T, int32_t *counters, int32_t *long_run,
-                                                    int32_t *long_chunk_base,
-                                                    int32_t *chunk_owner, int32_t *chunk_desc,
-                                                    int32_t *arrive, int sl_threshold, int chunk) {
-    const int U = counters[C_NUM_UNIQUE];
+// Each chunk slot then gets a descriptor -- its position range, key, table,
+// long run, the run's first slot and chunk count, and the batch window of
+// its first lookup's bag -- so the long-run kernel reads one 32-byte record
+// per chunk.  With ordering on, each chunk is also counted in its window.
+struct RouteParams {
+    const int32_t *seg_off;
+    const uint32_t *unique_keys;
+    const uint32_t *vals;
+    const int32_t *bag_of;
+    const int64_t *table_offset;
+    int64_t B;
+    int T;
+    int payload_pos;
+    int wshift;         // < 0: no ordering
+    int32_t *counters;
+    int32_t *long_run;
+    int32_t *long_chunk_base;
+    int32_t *chunk_desc;
+    int32_t *owner;     // [max_chunks] long run of each slot (the order array's memory)
+    int32_t *arrive;
+    int32_t *win;       // [CHUNK_WINDOWS_MAX] chunks per window (zeroed before)
+    int sl_threshold;
+    int chunk;
+};
+
+__global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
+    const int U = p.counters[C_NUM_UNIQUE];
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < U; r += gridDim.x * blockDim.x) {
-        const int32_t rs = seg_off[r], re = seg_off[r + 1];
+        const int32_t rs = p.seg_off[r], re = p.seg_off[r + 1];
         const int len = re - rs;
-        if (len < sl_threshold) continue;
-        const int nch = (len + chunk - 1) / chunk;
-        const int l = atomicAdd(counters + C_NUM_LONG, 1);
-        const int cb = atomicAdd(counters + C_NUM_CHUNKS, nch);
-        const uint32_t key = unique_keys[r];
-        const int t = table_of_key(table_offset, T, key);
-        long_run[l] = r;
-        long_chunk_base[l] = cb;
-        arrive[l] = 0;
-        for (int c = 0; c < nch; ++c) {
-            chunk_owner[cb + c] = l;
-            const int32_t s = rs + c * chunk;
-            int4 *d = reinterpret_cast<int4 *>(chunk_desc + (int64_t)(cb + c) * 8);
-            d[0] = make_int4(s, min(s + chunk, re), (int)key, t);
-            d[1] = make_int4(l, cb, nch, 0);
-        }
+        if (len < p.sl_threshold) continue;
+        const int nch = (len + p.chunk - 1) / p.chunk;
+        const int l = atomicAdd(p.counters + C_NUM_LONG, 1);
+        const int cb = atomicAdd(p.counters + C_NUM_CHUNKS, nch);
+        p.long_run[l] = r;
+        p.long_chunk_base[l] = cb;
+        p.arrive[l] = 0;
+        for (int c = 0; c < nch; ++c) p.owner[cb + c] = l;
     }
+}
+
+// One thread per chunk slot: the slot's descriptor and, with ordering on,
+// its window key t * windows_per_table + (first bag >> shift) (counted per
+// CTA in shared memory, then added globally).  Ordering by key makes the
+// warps of the long-run kernel work on one table's gradient rows of nearby
+// bags at a time, a working set that L2 holds.
+__global__ void __launch_bounds__(256) chunk_desc_kernel(const RouteParams p) {
+    __shared__ int32_t wc[CHUNK_WINDOWS_MAX];
+    const int wpt = p.wshift >= 0 ? (int)((p.B + (int64_t(1) << p.wshift) - 1) >> p.wshift) : 0;
+    const int nwin = p.T * wpt;
+    for (int i = threadIdx.x; i < nwin; i += blockDim.x) wc[i] = 0;
+    __syncthreads();
+    const int n = p.counters[C_NUM_CHUNKS];
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n; c += gridDim.x * blockDim.x) {
+        const int l = __ldg(p.owner + c);
+        const int r = __ldg(p.long_run + l);
+        const int cb = __ldg(p.long_chunk_base + l);
+        const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
+        const uint32_t key = __ldg(p.unique_keys + r);
+        const int t = table_of_key(p.table_offset, p.T, key);
+        const int32_t s = rs + (c - cb) * p.chunk;
+        int w = 0;
+        if (p.wshift >= 0) {
+            const uint32_t v = __ldg(p.vals + s);
+            int64_t b = p.payload_pos ? (int64_t)__ldg(p.bag_of + v) - (int64_t)t * p.B : (int64_t)v;
+            if (b < 0 || b >= p.B) b = 0;   // malformed offsets only
+            w = t * wpt + (int)(b >> p.wshift);
+            atomicAdd(wc + w, 1);
+        }
+        int4 *d = reinterpret_cast<int4 *>(p.chunk_desc + (int64_t)c * 8);
+        d[0] = make_int4(s, min(s + p.chunk, re), (int)key, t);
+        d[1] = make_int4(l, cb, (re - rs + p.chunk - 1) / p.chunk, w);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nwin; i += blockDim.x)
+        if (wc[i]) atomicAdd(p.win + i, wc[i]);
+}
+
+// Exclusive scan of the window counts, in place (one CTA).
+__global__ void __launch_bounds__(1024) chunk_window_scan_kernel(int32_t *win, int nwin) {
+    __shared__ int tot[32];
+    constexpr int PER = CHUNK_WINDOWS_MAX / 1024;
+    int v[PER], x = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int w = threadIdx.x * PER + i;
+        v[i] = w < nwin ? win[w] : 0;
+        x += v[i];
+    }
+    int total;
+    int run = block_excl_scan(x, tot, total);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int w = threadIdx.x * PER + i;
+        if (w < nwin) win[w] = run;
+        run += v[i];
+    }
+}
+
+// chunk_order[window start + k] = slot: slots grouped by window.
+__global__ void __launch_bounds__(256) chunk_order_kernel(const int32_t *__restrict__ chunk_desc,
+                                                          const int32_t *counters, int32_t *win,
+                                                          int32_t *chunk_order) {
+    const int n = counters[C_NUM_CHUNKS];
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n; c += gridDim.x * blockDim.x) {
+        const int w = __ldg(chunk_desc + (int64_t)c * 8 + 7);
+        chunk_order[atomicAdd(win + w, 1)] = c;
+    }
+}
+
+__global__ void zero_words_kernel(int32_t *p, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
 }
 
 __global__ void zero_counters_kernel(int32_t *counters) {
@@ -158,41 +249,77 @@ __global__ void zero_counters_kernel(int32_t *counters) {
 
 __global__ void zero_first_kernel(int32_t *p) { p[0] = 0; }
 
-tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_t sentinel,
-                      uint32_t *unique_keys, int32_t *seg_off, int32_t *counters,
-                      int32_t *long_run, int32_t *long_chunk_base, int32_t *chunk_owner,
-                      int32_t *chunk_desc, int32_t *arrive, const int64_t *table_offset, int T,
-                      int sl_threshold, int chunk, void *ws) {
+tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     L.before("tbe_rle_zero");
-    zero_counters_kernel<<<1, 32, 0, L.stream>>>(counters);
+    zero_counters_kernel<<<1, 32, 0, L.stream>>>(a.counters);
     L.after();
-    if (N == 0) {
+    if (a.N == 0) {
         // seg_off[0] = 0 for an empty batch
         L.before("tbe_rle_zero");
-        zero_first_kernel<<<1, 1, 0, L.stream>>>(seg_off);
+        zero_first_kernel<<<1, 1, 0, L.stream>>>(a.seg_off);
         L.after();
         return TBE_OK;
     }
-    const int64_t ntiles = (N + RLE_TILE - 1) / RLE_TILE;
+    const int64_t ntiles = (a.N + RLE_TILE - 1) / RLE_TILE;
     int32_t *tile_heads = (int32_t *)ws;
+    int32_t *win = (int32_t *)((char *)ws + ((size_t)(ntiles + 1) * 4 + 255) / 256 * 256);
+    const bool order = chunk_order_on(a.B);
+    const int wshift = order ? chunk_window_shift(a.B, a.T) : -1;
+    const int nwin = order ? a.T * (int)((a.B + (int64_t(1) << wshift) - 1) >> wshift) : 0;
     L.before("tbe_rle_count");
-    rle_count_kernel<<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(sorted_keys, N, sentinel,
-                                                                     tile_heads, counters);
+    rle_count_kernel<<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(a.sorted_keys, a.N, a.sentinel,
+                                                                     tile_heads, a.counters);
     L.after();
     L.before("tbe_rle_scan");
-    rle_scan_kernel<<<1, 1024, 0, L.stream>>>(tile_heads, ntiles, counters);
+    rle_scan_kernel<<<1, 1024, 0, L.stream>>>(tile_heads, ntiles, a.counters);
     L.after();
     L.before("tbe_rle_write");
     rle_write_kernel<<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
-        sorted_keys, N, sentinel, tile_heads, unique_keys, seg_off, counters);
+        a.sorted_keys, a.N, a.sentinel, tile_heads, a.unique_keys, a.seg_off, a.counters);
     L.after();
-    int grid = (int)((N + 255) / 256);
+    if (order) {
+        L.before("tbe_rle_zero");
+        zero_words_kernel<<<(nwin + 255) / 256, 256, 0, L.stream>>>(win, nwin);
+        L.after();
+    }
+    RouteParams p;
+    p.seg_off = a.seg_off;
+    p.unique_keys = a.unique_keys;
+    p.vals = a.sorted_vals;
+    p.bag_of = a.bag_of;
+    p.table_offset = a.table_offset;
+    p.B = a.B;
+    p.T = a.T;
+    p.payload_pos = a.payload_pos;
+    p.wshift = wshift;
+    p.counters = a.counters;
+    p.long_run = a.long_run;
+    p.long_chunk_base = a.long_chunk_base;
+    p.chunk_desc = a.chunk_desc;
+    p.owner = a.chunk_order;   // overwritten by the order kernel after its last use
+    p.arrive = a.arrive;
+    p.win = win;
+    p.sl_threshold = a.sl_threshold;
+    p.chunk = a.chunk;
+    int grid = (int)((a.N + 255) / 256);
     if (grid > L.num_sms * 8) grid = L.num_sms * 8;
     L.before("tbe_route");
-    route_kernel<<<grid, 256, 0, L.stream>>>(seg_off, unique_keys, table_offset, T, counters,
-                                             long_run, long_chunk_base, chunk_owner, chunk_desc,
-                                             arrive, sl_threshold, chunk);
+    route_kernel<<<grid, 256, 0, L.stream>>>(p);
     L.after();
+    int cg = (int)((a.N / 256 + 255) / 256);
+    if (cg > L.num_sms * 4) cg = L.num_sms * 4;
+    if (cg < 1) cg = 1;
+    L.before("tbe_chunk_desc");
+    chunk_desc_kernel<<<cg, 256, 0, L.stream>>>(p);
+    L.after();
+    if (order) {
+        L.before("tbe_chunk_window_scan");
+        chunk_window_scan_kernel<<<1, 1024, 0, L.stream>>>(win, nwin);
+        L.after();
+        L.before("tbe_chunk_order");
+        chunk_order_kernel<<<cg, 256, 0, L.stream>>>(a.chunk_desc, a.counters, win, a.chunk_order);
+        L.after();
+    }
     return TBE_OK;
 }
 

@@ -123,7 +123,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Meta layout (each array 256-byte aligned).
 struct MetaLayout {
     size_t keys_a, vals_a, keys_b, vals_b, bag_of, unique_keys, seg_off, counters, long_run,
-        long_chunk_base, arrive, chunk_owner, chunk_desc, hist, total;
+        long_chunk_base, arrive, chunk_order, chunk_desc, hist, total;
 };
 
 static MetaLayout meta_layout(const Problem &pr) {
@@ -148,12 +148,12 @@ static MetaLayout meta_layout(const Problem &pr) {
         m.long_run = take((size_t)pr.max_long * 4);
         m.long_chunk_base = take((size_t)pr.max_long * 4);
         m.arrive = take((size_t)pr.max_long * 4);
-        m.chunk_owner = take((size_t)pr.max_chunks * 4);
+        m.chunk_order = take((size_t)pr.max_chunks * 4);
         m.chunk_desc = take((size_t)pr.max_chunks * 32);
         m.hist = (size_t)-1;
     } else {
         m.keys_a = m.vals_a = m.keys_b = m.vals_b = m.bag_of = m.unique_keys = m.seg_off =
-            m.long_run = m.long_chunk_base = m.arrive = m.chunk_owner = m.chunk_desc = (size_t)-1;
+            m.long_run = m.long_chunk_base = m.arrive = m.chunk_order = m.chunk_desc = (size_t)-1;
         m.counters = take(C_COUNT * 4);
         m.hist = take((size_t)pr.NB * 64 * 2);
     }
@@ -204,10 +204,27 @@ static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batc
     if (st != TBE_OK) return st;
     meta->sorted_keys = in_b ? meta->keys_b : meta->keys_a;
     meta->sorted_vals = in_b ? meta->vals_b : meta->vals_a;
-    return launch_rle(L, meta->sorted_keys, pr.N, (uint32_t)pr.rows_total, meta->unique_keys,
-                      meta->seg_off, meta->counters, meta->long_run, meta->long_chunk_base,
-                      meta->chunk_owner, meta->chunk_desc, meta->arrive, tab->table_offset,
-                      tab->T, pr.sl_threshold, pr.chunk, ws);
+    RleArgs a;
+    a.sorted_keys = meta->sorted_keys;
+    a.sorted_vals = meta->sorted_vals;
+    a.bag_of = meta->bag_of;
+    a.N = pr.N;
+    a.B = pr.B;
+    a.sentinel = (uint32_t)pr.rows_total;
+    a.payload_pos = meta->payload_is_pos;
+    a.unique_keys = meta->unique_keys;
+    a.seg_off = meta->seg_off;
+    a.counters = meta->counters;
+    a.long_run = meta->long_run;
+    a.long_chunk_base = meta->long_chunk_base;
+    a.chunk_order = meta->chunk_order;
+    a.chunk_desc = meta->chunk_desc;
+    a.arrive = meta->arrive;
+    a.table_offset = tab->table_offset;
+    a.T = tab->T;
+    a.sl_threshold = pr.sl_threshold;
+    a.chunk = pr.chunk;
+    return launch_rle(L, a, ws);
 }
 
 }  // namespace tbe
@@ -272,7 +289,7 @@ tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes, const t
     meta->counters = (int32_t *)at(L.counters);
     meta->long_run = (int32_t *)at(L.long_run);
     meta->long_chunk_base = (int32_t *)at(L.long_chunk_base);
-    meta->chunk_owner = (int32_t *)at(L.chunk_owner);
+    meta->chunk_order = (int32_t *)at(L.chunk_order);
     meta->chunk_desc = (int32_t *)at(L.chunk_desc);
     meta->hist = (uint16_t *)at(L.hist);
     meta->bytes = L.total;

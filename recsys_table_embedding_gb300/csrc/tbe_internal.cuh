@@ -138,11 +138,38 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
 
 // --- rle.cu: run-length encode sorted keys, route long runs into chunks.
 size_t rle_workspace_bytes(int64_t N);
-tbe_status launch_rle(Launch &L, const uint32_t *sorted_keys, int64_t N, uint32_t sentinel,
-                      uint32_t *unique_keys, int32_t *seg_off, int32_t *counters,
-                      int32_t *long_run, int32_t *long_chunk_base, int32_t *chunk_owner,
-                      int32_t *chunk_desc, int32_t *arrive, const int64_t *table_offset, int T,
-                      int sl_threshold, int chunk, void *ws);
+// Long-run chunk slots are taken in order of (table, batch window of 2^wshift
+// bags of their first lookup) when the batch has at least CHUNK_ORDER_MIN_B
+// bags per table, so that concurrently reduced chunks share gradient rows.
+#ifndef TBE_CHUNK_ORDER_MIN_B
+#define TBE_CHUNK_ORDER_MIN_B 4096
+#endif
+constexpr int64_t CHUNK_ORDER_MIN_B = TBE_CHUNK_ORDER_MIN_B;
+constexpr int CHUNK_WINDOWS_MAX = 4096;
+bool chunk_order_on(int64_t B);
+int chunk_window_shift(int64_t B, int T);
+
+struct RleArgs {
+    const uint32_t *sorted_keys;
+    const uint32_t *sorted_vals;
+    const int32_t *bag_of;
+    int64_t N, B;
+    uint32_t sentinel;
+    int payload_pos;
+    uint32_t *unique_keys;
+    int32_t *seg_off;
+    int32_t *counters;
+    int32_t *long_run;
+    int32_t *long_chunk_base;
+    int32_t *chunk_order;
+    int32_t *chunk_desc;
+    int32_t *arrive;
+    const int64_t *table_offset;
+    int T;
+    int sl_threshold;
+    int chunk;
+};
+tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws);
 
 // --- backward.cu
 struct BwdArgs {

@@ -66,7 +66,7 @@ class tbe_meta(ctypes.Structure):
                 ("payload_is_pos", i32), ("key_bits", i32), ("rows_total", i64),
                 ("sorted_keys", P), ("sorted_vals", P), ("keys_a", P), ("vals_a", P),
                 ("keys_b", P), ("vals_b", P), ("bag_of", P), ("unique_keys", P), ("seg_off", P),
-                ("counters", P), ("long_run", P), ("long_chunk_base", P), ("chunk_owner", P),
+                ("counters", P), ("long_run", P), ("long_chunk_base", P), ("chunk_order", P),
                 ("arrive", P), ("chunk_desc", P), ("hist", P), ("bytes", ctypes.c_size_t)]
 
 

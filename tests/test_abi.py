@@ -67,7 +67,7 @@ def test_query_sizes_and_meta_bind_layout():
     assert m.bound_N == 10000 and m.path == 1 and m.payload_is_pos == 0
     assert m.rows_total == 2000 and m.key_bits == 11     # sentinel 2000 needs 11 bits
     ptrs = [m.keys_a, m.vals_a, m.keys_b, m.vals_b, m.unique_keys, m.seg_off, m.counters,
-            m.long_run, m.long_chunk_base, m.chunk_owner, m.arrive, m.chunk_desc]
+            m.long_run, m.long_chunk_base, m.chunk_order, m.arrive, m.chunk_desc]
     assert all(p % 256 == 0 and FAKE <= p < FAKE + mb for p in ptrs)
     assert len(set(ptrs)) == len(ptrs)
     assert m.bag_of is None and m.hist is None

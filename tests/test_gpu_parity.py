@@ -147,3 +147,42 @@ def test_bad_offsets_flagged_and_treated_empty():
     ref, _, _, bad = oracle.forward(wl, W.cpu().numpy())
     assert bad == 1
     np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("B", [4096, 3000])
+def test_chunk_descriptors_and_window_order(B):
+    # every chunk slot's descriptor against the runs of the oracle's
+    # inversion; with B >= 4096 the order is a permutation of the slots whose
+    # (table, 512-bag window) keys never decrease
+    from recsys_table_embedding_gb300 import meta_view
+    wl = workloads.large(B=B, E=20000)
+    W0, G, m0 = wl.weights(), wl.grad_out(), _m0(wl)
+    res = run_cuda(wl, W0, G, m0)
+    check_full(wl, W0, G, m0, res)
+    m = res["tbe"].meta
+    nch = res["num_chunks"]
+    assert nch > 0
+    desc = meta_view(m, "chunk_desc", nch * 8).cpu().numpy().reshape(nch, 8).astype(np.int64)
+    order = meta_view(m, "chunk_order", nch).cpu().numpy().astype(np.int64)
+    seg = res["seg_off"].astype(np.int64)
+    keys = res["unique_keys"].astype(np.int64)
+    vals = res["sorted_vals"].astype(np.int64)
+    runs = np.searchsorted(seg, desc[:, 0], side="right") - 1
+    rs, re = seg[runs], seg[runs + 1]
+    assert np.all(re - rs >= 256)
+    assert np.all((desc[:, 0] - rs) % 256 == 0)
+    np.testing.assert_array_equal(desc[:, 1], np.minimum(desc[:, 0] + 256, re))
+    np.testing.assert_array_equal(desc[:, 2], keys[runs])
+    np.testing.assert_array_equal(desc[:, 3], np.searchsorted(wl.table_offset, keys[runs], side="right") - 1)
+    np.testing.assert_array_equal(desc[:, 6], (re - rs + 255) // 256)
+    slot = np.arange(nch)
+    assert np.all((desc[:, 5] <= slot) & (slot < desc[:, 5] + desc[:, 6]))
+    np.testing.assert_array_equal(slot - desc[:, 5], (desc[:, 0] - rs) // 256)
+    assert len(np.unique(desc[:, 4])) == res["num_long"]
+    if B >= 4096:
+        # key = table * windows per table + (first bag >> 9): payload = bag
+        np.testing.assert_array_equal(desc[:, 7], desc[:, 3] * ((B + 511) // 512) + (vals[desc[:, 0]] >> 9))
+        np.testing.assert_array_equal(np.sort(order), slot)
+        assert np.all(np.diff(desc[order, 7]) >= 0)
+    else:
+        assert np.all(desc[:, 7] == 0)
