@@ -13,8 +13,9 @@
 //     CTA only ever waits for tiles that CTAs already running hold).  A tile
 //     of 4096 pairs is ranked stably inside the CTA (per-warp match_any
 //     ranking in input order, then warp prefixes), each digit's tile count is
-//     published, and thread d (one per bucket) looks back over earlier tiles for digit d's
-//     running prefix.  The tile is reordered by digit in shared memory and
+//     published, and thread d (one per bucket) looks back over earlier
+//     tiles for digit d's running prefix, reading LOOKBACK predecessors per
+//     round trip.  The tile is reordered by digit in shared memory and
 //     written out, so each digit's run of pairs lands contiguously.
 //  The look-back status word packs a 2-bit state and a 30-bit count (so
 //  N < 2^30).  Every wait is bounded: after WAIT_LIMIT_NS of polling the CTA
@@ -34,6 +35,10 @@ constexpr uint32_t ST_AGG = 1u << 30;
 constexpr uint32_t ST_INC = 2u << 30;
 constexpr uint32_t ST_MASK = (1u << 30) - 1;
 constexpr int MAX_PASSES = 4;
+#ifndef TBE_SORT_LOOKBACK
+#define TBE_SORT_LOOKBACK 8
+#endif
+constexpr int LOOKBACK = TBE_SORT_LOOKBACK;   // predecessors read per look-back round trip
 
 static int num_passes(int key_bits) { return (key_bits + MAX_DIGIT_BITS - 1) / MAX_DIGIT_BITS; }
 static int digit_bits(int key_bits) {
@@ -190,12 +195,30 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
             st_relaxed_u32(st, ST_INC | sum);
         } else {
             st_relaxed_u32(st, ST_AGG | sum);
+            // look back LOOKBACK predecessors per round trip: add aggregates
+            // in order until an inclusive prefix (or tile 0); stop at the
+            // first tile that has published nothing yet and poll it again
             int64_t j = tile - 1;
             uint64_t t0 = 0;
             while (true) {
-                const uint32_t s = ld_relaxed_u32(status + j * RADIX + d);
-                const uint32_t f = s & ~ST_MASK;
-                if (f == 0) {
+                uint32_t sv[LOOKBACK];
+#pragma unroll
+                for (int q = 0; q < LOOKBACK; ++q)
+                    sv[q] = j - q >= 0 ? ld_relaxed_u32(status + (j - q) * RADIX + d) : 0u;
+                int used = 0;
+                bool done = false;
+#pragma unroll
+                for (int q = 0; q < LOOKBACK; ++q) {
+                    if (done || used < q) break;
+                    const uint32_t f = sv[q] & ~ST_MASK;
+                    if (f == 0) break;
+                    excl += sv[q] & ST_MASK;
+                    used = q + 1;
+                    done = f == ST_INC || j - q == 0;
+                }
+                if (done) break;
+                j -= used;
+                if (used == 0) {
                     const uint64_t now = global_ns();
                     if (t0 == 0) t0 = now;
                     else if (now - t0 > WAIT_LIMIT_NS) {
@@ -203,11 +226,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
                         break;
                     }
                     __nanosleep(64);
-                    continue;
                 }
-                excl += s & ST_MASK;
-                if (f == ST_INC || j == 0) break;
-                --j;
             }
             st_relaxed_u32(st, ST_INC | (excl + sum));
         }
