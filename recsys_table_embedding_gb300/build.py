@@ -39,8 +39,22 @@ def _deps():
         os.path.join(INCLUDE, "tbe.h")]
 
 
+STAMP = os.path.join(BUILD, "flags.txt")
+
+
+def _flags() -> list:
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+                    "-I", CSRC, "--expt-relaxed-constexpr", "-Xcompiler", "-Wall"]
+    # tuning knobs (-DTBE_FWD_ROWS=...), e.g. for launch-shape sweeps
+    return flags + os.environ.get("TBE_NVCC_DEFINES", "").split()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    """The library exists, is newer than every source, and was built with the
+    same compiler flags (tuning knobs included)."""
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+        return False
+    if open(STAMP).read() != " ".join(_flags()):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
@@ -51,12 +65,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                    "-I", CSRC, "--expt-relaxed-constexpr", "-Xcompiler", "-Wall"]
+    flags = _flags()
     if os.environ.get("TBE_PTXAS_VERBOSE"):
         flags += ["-Xptxas", "-v"]
-    # tuning knobs (-DTBE_FWD_ROWS=...), e.g. for launch-shape sweeps
-    flags += os.environ.get("TBE_NVCC_DEFINES", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
@@ -76,6 +87,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(_flags()))
     return LIB
 
 

@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
     unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * warp_smem_bytes(p.chunk);
     const uint32_t ring0 = smem_addr(wsm);
     const uint32_t bar0 = smem_addr(wsm + STAGES * STAGE_BYTES);
-    uint32_t *offb = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);  // [2][chunk]
+    uint32_t *offb = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);  // [2][chunk], 16-B units
     float *wgt = reinterpret_cast<float *>(offb + 2 * p.chunk);                       // [2][chunk]
     if (lane == 0)
         for (int i = 0; i < STAGES; ++i) bar_init(bar0 + 8 * i, 1);
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             pv[k] = i < c.e ? __ldg(p.vals + i) : 0u;
         }
     };
-    // element offset (from G_t) and weight of each lookup of c into buffer buf
+    // offset from G_t (in 16-byte vectors) and weight of each lookup of c into buffer buf
     auto stage = [&](const Chunk &c, int buf) {
         const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + c.t) != 0);
         const int64_t tB = (int64_t)c.t * p.B;
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             // only malformed (overlapping) offsets can give a bag outside the
             // run's table: such a lookup copies row 0 with weight 0
             const bool ok = b >= 0 && (int64_t)b < p.B;
-            o[i] = ok ? (uint32_t)((int64_t)b * rowstride) : 0u;
+            o[i] = ok ? (uint32_t)(((int64_t)b * rowstride) >> 2) : 0u;   // 16-byte units
             w[i] = ok ? x : 0.f;
         };
 #pragma unroll
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         const uint32_t bar = bar0 + 8 * st;
         if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
         __syncwarp();
-        const float *Gt = p.G + (int64_t)c.t * p.D;
+        const float4 *Gt = reinterpret_cast<const float4 *>(p.G + (int64_t)c.t * p.D);
         const uint32_t *o = offb + buf * p.chunk + k * R;
         const uint32_t dst0 = ring0 + st * STAGE_BYTES;
         for (int j = lane; j < rows; j += 32) bulk_g2s(dst0 + j * row_bytes, Gt + o[j], row_bytes, bar);
@@ -581,6 +581,338 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
     }
 }
 
+// ---- streaming short runs (gradient rows of 512 bytes and more) -----------
+// A warp takes tasks of RT consecutive runs (lane i: run r0 + i), skips the
+// long ones, and streams the gradient rows of the short ones, in sorted
+// order, through the same kind of bulk-copy ring as the long-run kernel.
+// The lookups of a task are staged 32 at a time into a table (offset,
+// weight, run slot, last-of-run flag); each run's weight row is copied into a
+// per-task shared buffer and its momentum loaded when the task starts, so the
+// Adagrad update of a run is applied as soon as its last gradient row has
+// been added, without a round trip to memory.  The ring, the tables and the
+// weight buffers are double-buffered across blocks and tasks, so metadata,
+// payload and weight loads overlap the rows in flight.
+
+#ifndef TBE_SHORT_STREAM
+#define TBE_SHORT_STREAM 1   // 0: the register kernel for every row size
+#endif
+#ifndef TBE_SHORT_STAGES
+#define TBE_SHORT_STAGES 3
+#endif
+constexpr int SS_STAGES = TBE_SHORT_STAGES;
+constexpr int SS_WARPS = 2;          // warps per CTA
+#ifndef TBE_SHORT_WBUF
+#define TBE_SHORT_WBUF 4096
+#endif
+constexpr int SS_WBUF = TBE_SHORT_WBUF;   // weight-row buffer per task
+constexpr int SS_BLK = 32;           // lookups per staged table
+constexpr uint32_t SS_LAST = 0x100u; // tag flag: last lookup of its run
+
+__host__ __device__ constexpr int ss_warp_bytes() {
+    return (SS_STAGES * STAGE_BYTES + 2 * SS_WBUF + 3 * 2 * SS_BLK * 4 + 8 * (SS_STAGES + 2) + 127) /
+           128 * 128;
+}
+// runs per task: as many weight rows as fit the buffer, at most 32
+__host__ __device__ inline int ss_runs_per_task(int wrow_bytes) {
+    const int r = SS_WBUF / wrow_bytes;
+    return r < 1 ? 1 : (r > 32 ? 32 : r);
+}
+
+// One task as its lanes hold it (lane i: run r0 + i).
+struct SsTask {
+    int q;          // task index (-1: none)
+    int nr;         // runs in the task
+    int32_t s;      // first sorted position of the lane's run
+    int32_t e;
+    uint32_t key;
+    int len;        // lookups of the lane's run if short, else 0
+    int pre;        // exclusive prefix of len over the lanes
+    int total;      // short-run lookups of the task
+    int t;          // table of the lane's run
+    float mom;      // momentum of the lane's row
+};
+
+template <typename WT, int NV>
+__global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(const BwdParams p) {
+    using ACC = typename WTraits<WT>::acc;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int U_runs = p.counters[C_NUM_UNIQUE];
+    const int wrow = p.D * (int)sizeof(WT);
+    const int RT = ss_runs_per_task(wrow);
+    const int ntasks = (U_runs + RT - 1) / RT;
+    const int q0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (q0 >= ntasks) return;
+
+    unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * ss_warp_bytes();
+    unsigned char *ring = wsm;
+    unsigned char *wbuf = ring + SS_STAGES * STAGE_BYTES;                  // [2][SS_WBUF]
+    uint32_t *tab_off = reinterpret_cast<uint32_t *>(wbuf + 2 * SS_WBUF);  // [2][32], 16-B units
+    float *tab_w = reinterpret_cast<float *>(tab_off + 2 * SS_BLK);        // [2][32]
+    uint32_t *tab_tag = reinterpret_cast<uint32_t *>(tab_w + 2 * SS_BLK);  // [2][32]
+    const uint32_t bar0 = smem_addr(tab_tag + 2 * SS_BLK);                 // ring stages
+    const uint32_t wbar0 = bar0 + 8 * SS_STAGES;                            // weight buffers
+    if (lane == 0)
+        for (int i = 0; i < SS_STAGES + 2; ++i) bar_init(bar0 + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    const uint32_t row_bytes = (uint32_t)p.D * 4;
+    const int R = STAGE_BYTES / (int)row_bytes;   // gradient rows per stage (1..8)
+    const int64_t TD = (int64_t)p.T * p.D;
+    const float4 *G4 = reinterpret_cast<const float4 *>(p.G);
+
+    // phase A: run bounds and keys of task q (loads only; lane i: run q*RT + i)
+    auto task_load = [&](int q, SsTask &T) {
+        T.q = q < ntasks ? q : -1;
+        T.nr = T.q >= 0 ? min(RT, U_runs - q * RT) : 0;
+        T.s = T.e = 0;
+        T.key = 0;
+        T.len = T.pre = T.total = T.t = 0;
+        T.mom = 0.f;
+        if (lane < T.nr) {
+            T.s = __ldg(p.seg_off + q * RT + lane);
+            T.e = __ldg(p.seg_off + q * RT + lane + 1);
+            T.key = __ldg(p.unique_keys + q * RT + lane);
+        }
+    };
+    // phase B: lengths of the short runs, prefixes, tables, momentum; the
+    // weight rows of the short runs are copied into weight buffer wb
+    uint32_t wphase = 0;   // bit k: parity of weight buffer k's next completion
+    auto task_prepare = [&](SsTask &T, int wb) {
+        const bool mine = T.q >= 0 && lane < T.nr && T.e - T.s < p.sl_threshold;
+        T.len = mine ? T.e - T.s : 0;
+        int x = T.len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        T.total = __shfl_sync(FULL, x, 31);
+        T.pre = x - T.len;
+        T.t = mine ? table_of_key(p.table_offset, p.T, T.key) : 0;
+        T.mom = mine ? p.mom[T.key] : 0.f;
+        const unsigned m = __ballot_sync(FULL, mine);
+        if (m) {
+            const uint32_t bar = wbar0 + 8 * wb;
+            if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)__popc(m) * (uint32_t)wrow);
+            __syncwarp();
+            if (mine)
+                bulk_g2s(smem_addr(wbuf + wb * SS_WBUF + lane * wrow),
+                         reinterpret_cast<const WT *>(p.W) + (int64_t)T.key * p.D, (uint32_t)wrow, bar);
+        }
+    };
+    // table of block blk of task T (its lookups blk*32 + lane) into buffer tb
+    auto stage_block = [&](const SsTask &T, int blk, int tb) {
+        const int k = blk * SS_BLK + lane;
+        // the lookup's run slot: the largest lane whose prefix is <= k (a
+        // zero-length slot is never the largest such lane for k < total)
+        int slot = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+            const int c = slot + step;
+            const int pre_c = __shfl_sync(FULL, T.pre, c & 31);
+            if (c < 32 && pre_c <= k) slot = c;
+        }
+        const int32_t s_sl = __shfl_sync(FULL, T.s, slot);
+        const int pre_sl = __shfl_sync(FULL, T.pre, slot);
+        const int len_sl = __shfl_sync(FULL, T.len, slot);
+        const int t_sl = __shfl_sync(FULL, T.t, slot);
+        if (k < T.total) {
+            const uint32_t v = __ldg(p.vals + s_sl + (k - pre_sl));
+            int b;
+            float x = 1.f;
+            if (p.payload_pos) {
+                b = (int)((int64_t)__ldg(p.bag_of + v) - (int64_t)t_sl * p.B);
+                if (p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t_sl) != 0))
+                    x = __ldg(p.psw + v);
+            } else {
+                b = (int)v;
+            }
+            // only malformed (overlapping) offsets can give a bag outside the
+            // run's table: such a lookup copies row 0 with weight 0
+            const bool ok = b >= 0 && (int64_t)b < p.B;
+            tab_off[tb * SS_BLK + lane] = ok ? (uint32_t)(((int64_t)b * TD + (int64_t)t_sl * p.D) >> 2) : 0u;
+            tab_w[tb * SS_BLK + lane] = ok ? x : 0.f;
+            tab_tag[tb * SS_BLK + lane] = (uint32_t)slot | (k == pre_sl + len_sl - 1 ? SS_LAST : 0u);
+        }
+        __syncwarp();
+    };
+    auto nblocks = [&](const SsTask &T) { return (T.total + SS_BLK - 1) / SS_BLK; };
+
+    uint32_t gprod = 0, gcons = 0, phase = 0;
+    auto produce = [&](const SsTask &T, int blk, int tb, int sb) {
+        const int st = (int)(gprod % SS_STAGES);
+        const int rows = min(R, T.total - blk * SS_BLK - sb * R);
+        const uint32_t bar = bar0 + 8 * st;
+        if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
+        __syncwarp();
+        const uint32_t dst0 = smem_addr(ring + st * STAGE_BYTES);
+        for (int j = lane; j < rows; j += 32)
+            bulk_g2s(dst0 + j * row_bytes, G4 + tab_off[tb * SS_BLK + sb * R + j], row_bytes, bar);
+        ++gprod;
+    };
+
+    // Tasks: cur (consumed now, weight buffer cw), nxt (prepared: weight rows
+    // copied into buffer cw ^ 1), nn (run bounds loaded).  Moving on makes nxt
+    // current and prepares the task after it into the buffer just released.
+    SsTask cur, nxt, nn;
+    int cw = 0;
+    task_load(q0, cur);
+    task_load(q0 + nwarps, nxt);
+    task_load(q0 + 2 * nwarps, nn);
+    task_prepare(cur, 0);
+    task_prepare(nxt, 1);
+    auto advance = [&]() {
+        cur = nxt;
+        cw ^= 1;
+        nxt = nn;
+        task_load(cur.q >= 0 ? cur.q + 2 * nwarps : ntasks, nn);
+        task_prepare(nxt, cw ^ 1);
+    };
+    while (cur.q >= 0 && cur.total == 0) advance();
+    if (cur.q < 0) return;
+
+    // Blocks are numbered in consumption order; block n uses table buffer n&1.
+    // consumer: block cn = block cblk of task cur
+    // staged:   the newest block whose table is staged (cn or cn + 1)
+    // producer: block pn (cn or cn + 1), next stage psb
+    int cblk = 0;
+    uint32_t cn = 0, staged = 0, pn = 0;
+    int psb = 0;
+    stage_block(cur, 0, 0);
+
+    auto refill = [&]() {
+        while (gprod - gcons < (uint32_t)SS_STAGES && pn <= staged) {
+            const bool in_cur = pn == cn || cblk + 1 < nblocks(cur);
+            const SsTask &T = in_cur ? cur : nxt;
+            const int blk = pn == cn ? cblk : (in_cur ? cblk + 1 : 0);
+            const int nsb = (min(SS_BLK, T.total - blk * SS_BLK) + R - 1) / R;
+            if (psb < nsb) {
+                produce(T, blk, (int)(pn & 1), psb++);
+                continue;
+            }
+            if (pn != cn) break;   // at most one block ahead of the consumer
+            ++pn;
+            psb = 0;
+        }
+    };
+    refill();
+
+    ACC acc[NV][4];
+#pragma unroll
+    for (int q = 0; q < NV; ++q)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+    bool wready = false;   // the current task's weight rows have landed
+
+    for (;;) {
+        // stage the table of the block after the consumer's
+        if (staged == cn) {
+            if (cblk + 1 < nblocks(cur)) {
+                stage_block(cur, cblk + 1, (int)((cn + 1) & 1));
+                staged = cn + 1;
+            } else if (nxt.q >= 0 && nxt.total > 0) {
+                stage_block(nxt, 0, (int)((cn + 1) & 1));
+                staged = cn + 1;
+            }
+        }
+        refill();
+        const int tb = (int)(cn & 1);
+        const int rows_blk = min(SS_BLK, cur.total - cblk * SS_BLK);
+        const int nsb = (rows_blk + R - 1) / R;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int st = (int)(gcons % SS_STAGES);
+            if (!mbar_wait_bounded(bar0 + 8 * st, (phase >> st) & 1u)) {
+                // stop issuing: give the copies still in flight one more
+                // bounded wait each, flag the failure, end the warp's work
+                for (uint32_t g = gcons + 1; g < gprod; ++g)
+                    mbar_wait_bounded(bar0 + 8 * (g % SS_STAGES), (phase >> (g % SS_STAGES)) & 1u);
+                if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
+                return;
+            }
+            phase ^= 1u << st;
+            const int rows = min(R, rows_blk - sb * R);
+            const unsigned char *sp = ring + st * STAGE_BYTES;
+            for (int j = 0; j < rows; ++j) {
+                const int e = tb * SS_BLK + sb * R + j;
+                const float x = tab_w[e];
+                const uint32_t tag = tab_tag[e];
+                const float4 *src = reinterpret_cast<const float4 *>(sp + j * row_bytes) + lane;
+#pragma unroll
+                for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * 32], x);
+                if (!(tag & SS_LAST)) continue;
+                // the run in slot (tag & 31) is complete: exact rowwise Adagrad
+                //   m += mean_d(g^2);  w -= lr * g / (sqrt(m) + eps)
+                if (!wready) {
+                    if (!mbar_wait_bounded(wbar0 + 8 * cw, (wphase >> cw) & 1u)) {
+                        for (uint32_t g = gcons + 1; g < gprod; ++g)
+                            mbar_wait_bounded(bar0 + 8 * (g % SS_STAGES), (phase >> (g % SS_STAGES)) & 1u);
+                        if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_COPY_TIMEOUT);
+                        return;
+                    }
+                    wphase ^= 1u << cw;
+                    wready = true;
+                }
+                const int slot = (int)(tag & 31u);
+                float gf[NV][4];
+                ACC ss = ACC(0);
+#pragma unroll
+                for (int q = 0; q < NV; ++q)
+#pragma unroll
+                    for (int x2 = 0; x2 < 4; ++x2) {
+                        gf[q][x2] = (float)acc[q][x2];
+                        ss += (ACC)gf[q][x2] * (ACC)gf[q][x2];
+                        acc[q][x2] = ACC(0);
+                    }
+#pragma unroll
+                for (int sh = 1; sh < 32; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
+                const float m_old = __shfl_sync(FULL, cur.mom, slot);
+                const uint32_t key = __shfl_sync(FULL, cur.key, slot);
+                const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
+                const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+                const WT *wsrc = reinterpret_cast<const WT *>(wbuf + cw * SS_WBUF + slot * wrow) + lane * 4;
+                WT *wdst = reinterpret_cast<WT *>(p.W) + (int64_t)key * p.D + lane * 4;
+#pragma unroll
+                for (int q = 0; q < NV; ++q) {
+                    float w[4];
+                    ld4(wsrc + q * 128, w);
+#pragma unroll
+                    for (int x2 = 0; x2 < 4; ++x2)
+                        w[x2] = __fsub_rn(w[x2], __fdiv_rn(__fmul_rn(p.lr, gf[q][x2]), den));
+                    st4(wdst + q * 128, w);
+                }
+                if (lane == 0) p.mom[key] = m_new;
+            }
+            ++gcons;
+            __syncwarp();   // the stage is read before it is refilled
+            refill();
+        }
+        if (cblk + 1 < nblocks(cur)) {
+            ++cblk;
+            ++cn;
+            continue;
+        }
+        // task done: the next task with short-run lookups becomes current
+        do {
+            advance();
+        } while (cur.q >= 0 && cur.total == 0);
+        if (cur.q < 0) break;
+        wready = false;
+        cblk = 0;
+        ++cn;
+        if (staged < cn) {   // empty tasks were skipped: the table is not staged yet
+            stage_block(cur, 0, (int)(cn & 1));
+            staged = cn;
+        }
+        if (pn < cn) {
+            pn = cn;
+            psb = 0;
+        }
+    }
+}
+
 template <typename WT, int LPR, int NV>
 __global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
@@ -648,16 +980,29 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     }
-    // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
-    constexpr int V = LPR * NV;                       // float4 vectors per gradient row
-    constexpr int SNV = short_vectors_per_lane(V);
-    constexpr int SGL = V / SNV;
-    static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0, "short-run lane groups");
-    constexpr int SU = SNV >= 3 ? 2 : 4;
-    auto ks = tbe_bwd_short_kernel<WT, SGL, SNV, SU>;
-    L.before("tbe_bwd_short_run");
-    ks<<<persistent_grid(ks, L.num_sms), 256, 0, L.stream>>>(p);
-    L.after();
+    if constexpr (LPR == 32 && TBE_SHORT_STREAM) {
+        // gradient rows of 512 bytes and more: short runs streamed through a
+        // bulk-copy ring, one row per warp step
+        auto ks = tbe_bwd_short_stream_kernel<WT, NV>;
+        const size_t ssm = (size_t)SS_WARPS * ss_warp_bytes();
+        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+        cudaFuncSetAttribute(ks, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        L.before("tbe_bwd_short_run");
+        ks<<<persistent_grid(ks, L.num_sms, ssm, SS_WARPS * 32), SS_WARPS * 32, ssm, L.stream>>>(p);
+        L.after();
+    } else {
+        // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
+        constexpr int V = LPR * NV;                       // float4 vectors per gradient row
+        constexpr int SNV = short_vectors_per_lane(V);
+        constexpr int SGL = V / SNV;
+        static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0, "short-run lane groups");
+        constexpr int SU = SNV >= 3 ? 2 : 4;
+        auto ks = tbe_bwd_short_kernel<WT, SGL, SNV, SU>;
+        L.before("tbe_bwd_short_run");
+        ks<<<persistent_grid(ks, L.num_sms), 256, 0, L.stream>>>(p);
+        L.after();
+    }
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto ka = tbe_bwd_apply_kernel<WT, LPR, NV>;
         L.before("tbe_bwd_apply");

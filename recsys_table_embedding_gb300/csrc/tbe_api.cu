@@ -115,6 +115,9 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     const int esz = tab->dtype == TBE_F32 ? 4 : 2;
     if (pr->path == 1 && (!row_plan(tab->D, esz).ok || !row_plan(tab->D, 4).ok))
         return TBE_ERR_UNSUPPORTED_DIM;
+    // the backward stages gradient-row offsets as 32-bit counts of 16-byte
+    // vectors: grad_out must stay under 64 GB
+    if (pr->path == 1 && pr->NB * tab->D / 4 >= (int64_t(1) << 32)) return TBE_ERR_INVALID_ARGUMENT;
     return TBE_OK;
 }
 

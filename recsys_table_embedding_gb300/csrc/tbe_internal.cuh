@@ -68,18 +68,24 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+#ifndef TBE_MBAR_SUSPEND_NS
+#define TBE_MBAR_SUSPEND_NS 20000
+#endif
 // Bounded wait for the completion of the mbarrier phase with the given parity
-// (shared-memory address `bar`).  False if WAIT_LIMIT_NS passed first.
+// (shared-memory address `bar`).  Each try_wait may suspend the thread for up
+// to TBE_MBAR_SUSPEND_NS until the phase completes, so a waiting warp does
+// not spin through issue slots the other warps need.  False if WAIT_LIMIT_NS
+// passed first.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "n"(TBE_MBAR_SUSPEND_NS)
             : "memory");
         if (ok) return true;
         const uint64_t now = global_ns();
