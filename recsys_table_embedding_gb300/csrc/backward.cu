@@ -163,14 +163,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 // own 16-byte vectors of each row from shared memory.
 
 #ifndef TBE_BWD_STAGES
-#define TBE_BWD_STAGES 3
+#define TBE_BWD_STAGES 2   // more warps beat deeper rings: 3.20 ms at 2 stages vs 3.96 at 3
 #endif
 #ifndef TBE_CHUNK_THREADS
 #define TBE_CHUNK_THREADS 128
 #endif
 constexpr int STAGES = TBE_BWD_STAGES;
 constexpr int STAGE_BYTES = 4096;
-constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;   // 4 warps: three blocks fit an SM at chunk 256
+constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;   // 4 warps: four blocks fit an SM at chunk 256
 constexpr int PV = 8;                // payloads a lane prefetches in registers
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
@@ -594,15 +594,15 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 // payload and weight loads overlap the rows in flight.
 
 #ifndef TBE_SHORT_STREAM
-#define TBE_SHORT_STREAM 1   // 0: the register kernel for every row size
+#define TBE_SHORT_STREAM 1   // 0: the register kernel for every batch
 #endif
 #ifndef TBE_SHORT_STAGES
-#define TBE_SHORT_STAGES 3
+#define TBE_SHORT_STAGES 1   // mid workload: 1.93 ms at 1 stage, 2.18 at 2, 2.59 at 3 (more warps win)
 #endif
 constexpr int SS_STAGES = TBE_SHORT_STAGES;
 constexpr int SS_WARPS = 2;          // warps per CTA
 #ifndef TBE_SHORT_WBUF
-#define TBE_SHORT_WBUF 4096
+#define TBE_SHORT_WBUF 2048   // mid workload: 2.02 ms at 2 KB vs 2.18 at 4 KB (2 stages)
 #endif
 constexpr int SS_WBUF = TBE_SHORT_WBUF;   // weight-row buffer per task
 constexpr int SS_BLK = 32;           // lookups per staged table
@@ -980,9 +980,15 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     }
-    if constexpr (LPR == 32 && TBE_SHORT_STREAM) {
-        // gradient rows of 512 bytes and more: short runs streamed through a
-        // bulk-copy ring, one row per warp step
+    bool stream = false;
+    if constexpr (LPR == 32 && TBE_SHORT_STREAM) stream = p.payload_pos != 0;
+    if (stream) {
+        // weighted batch, gradient rows of 512 bytes and more: short runs
+        // streamed through a bulk-copy ring, one row per warp step; staging
+        // 32 lookups at a time amortises the dependent bag lookup of a
+        // position payload (2.60 vs 2.82 ms on the mid workload, while the
+        // register kernel stays ahead on unweighted batches, 2.55 vs 2.80 ms
+        // on the large one)
         auto ks = tbe_bwd_short_stream_kernel<WT, NV>;
         const size_t ssm = (size_t)SS_WARPS * ss_warp_bytes();
         cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
@@ -991,7 +997,8 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         L.before("tbe_bwd_short_run");
         ks<<<persistent_grid(ks, L.num_sms, ssm, SS_WARPS * 32), SS_WARPS * 32, ssm, L.stream>>>(p);
         L.after();
-    } else {
+    }
+    if (!stream) {
         // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
         constexpr int V = LPR * NV;                       // float4 vectors per gradient row
         constexpr int SNV = short_vectors_per_lane(V);
