@@ -186,3 +186,17 @@ def test_chunk_descriptors_and_window_order(B):
         assert np.all(np.diff(desc[order, 7]) >= 0)
     else:
         assert np.all(desc[:, 7] == 0)
+
+
+@pytest.mark.parametrize("dtype,D", [("f16", 128), ("f32", 256)])
+def test_weighted_short_runs_around_long_runs(dtype, D):
+    # weighted batch with gradient rows >= 512 B: short runs take the
+    # streaming kernel.  Table 0 has 24 rows, each looked up ~1300 times
+    # (long runs only: whole tasks of the short-run kernel are empty), table 1
+    # has 6000 rows (short runs), table 2 mixes both
+    wl = workloads.make_workload("mixw", T=3, table_rows=[24, 6000, 300], D=D, dtype=dtype, B=4096,
+                                 lengths=("poisson", 8.0), dist=("zipf", 1.1), seed=21,
+                                 weighted=[True, True, True], oob_frac=0.01)
+    res = _step(wl)
+    assert res["num_long"] >= 24
+    assert res["payload_is_pos"] == 1
