@@ -55,7 +55,8 @@ extern "C" {
 typedef enum tbe_status {
     TBE_OK = 0,
     TBE_ERR_NULL_POINTER = 1,       /* a required pointer is NULL */
-    TBE_ERR_INVALID_ARGUMENT = 2,   /* T, B, N, D out of range, table_offset not monotone, ... */
+    TBE_ERR_INVALID_ARGUMENT = 2,   /* T, B, N, D out of range, table_offset not monotone,
+                                       grad_out of 64 GB or more on the generic path, ... */
     TBE_ERR_UNSUPPORTED_DIM = 3,    /* D*sizeof(weight) not one of the supported row sizes */
     TBE_ERR_UNSUPPORTED_DTYPE = 4,
     TBE_ERR_MISALIGNED = 5,         /* a device pointer is not 16-byte aligned */
@@ -228,7 +229,9 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
  * the short-run kernel; longer runs are reduced in 256-lookup chunks (two
  * kernels or one fused launch, cfg->long_run_mode).  Weighted tables scale
  * each gradient row by its per-sample weight before accumulation.
- * `batch` must be the one `meta` was filled from.
+ * `batch` must be the one `meta` was filled from.  On the generic path
+ * grad_out must be smaller than 64 GB (B*T*D < 2^34 elements): gradient-row
+ * offsets are staged as 32-bit counts of 16-byte vectors.
  */
 tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batch *batch,
                                         float *momentum, const float *grad_out,

@@ -82,6 +82,8 @@ def test_query_sizes_and_meta_bind_layout():
 @pytest.mark.parametrize("kw,code", [
     (dict(D=6), 3), (dict(D=4, dtype=1), 3), (dict(D=1024, dtype=0), 3), (dict(dtype=7), 4),
     (dict(N=1 << 30), 2), (dict(rows=[2**30, 2**30]), 6), (dict(rows=[5, -1]), 2),
+    # grad_out [B, T*D] float32 of 64 GB or more: gradient offsets would not fit 32 bits
+    (dict(T=2, B=2**27, D=128), 2), (dict(T=2, B=2**25, D=128), 0),
 ])
 def test_host_side_argument_errors(kw, code):
     f = Fake(**kw)
