@@ -347,10 +347,17 @@ def run_ours(args):
         kb = kernel_bytes(dom, wl, st, pif)
         if kb is not None:
             ach = kb / avg_s / 1e9
+            traffic = ncu_traffic(dom, args.workload)
             roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                     "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
-                    "traffic": ncu_traffic(dom, args.workload), "bytes_per_launch": kb,
+                    "traffic": traffic, "bytes_per_launch": kb,
                     "avg_launch_ms": round(avg_s * 1e3, 4), "peak_source": peak_src}
+            if traffic:
+                # what DRAM itself delivered: algorithmic bytes above count
+                # re-reads that L2 serves, so `frac` can exceed 1
+                dach = traffic / avg_s / 1e9
+                roof["dram_achieved"] = round(dach, 1)
+                roof["dram_frac"] = round(dach / hbm_peak, 4)
     step_ach = sb["total"] / (ms_step / 1e3) / 1e9
     kernels = {n: {"launches": c, "avg_ms": round(t / c, 4), "share": round(t / sum(v[1] for v in kern.values()), 4)}
                for n, (c, t) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
