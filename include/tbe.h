@@ -170,8 +170,8 @@ typedef struct tbe_meta {
     int32_t *long_chunk_base;           /* [max_long] first chunk slot of long run l */
     int32_t *chunk_order;               /* [max_chunks] chunk slot taken c-th by the long-run
                                            kernel: slots grouped by table and batch window of
-                                           their first lookup's bag (batches of B >= 4096); scratch
-                                           for smaller batches, whose slot c is taken c-th */
+                                           their first lookup's bag (B >= 4096 and T <= 4096);
+                                           scratch otherwise, and slot c is taken c-th */
     int32_t *arrive;                    /* [max_long] arrival counters of the fused long-run path */
     int32_t *chunk_desc;                /* [max_chunks][8] per chunk slot: first and end sorted
                                            position, key, table, long run, first slot of the run,

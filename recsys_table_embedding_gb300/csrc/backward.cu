@@ -1050,7 +1050,7 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.counters = m->counters;
     p.long_run = m->long_run;
     p.long_chunk_base = m->long_chunk_base;
-    p.chunk_order = chunk_order_on(a.bt->B) ? m->chunk_order : nullptr;
+    p.chunk_order = chunk_order_on(a.bt->B, a.tab->T) ? m->chunk_order : nullptr;
     p.chunk_desc = m->chunk_desc;
     p.partials = a.partials;
     p.arrive = a.arrive;

@@ -24,12 +24,16 @@ size_t rle_workspace_bytes(int64_t N) {
     return ((size_t)(ntiles + 1) * 4 + 255) / 256 * 256 + (size_t)CHUNK_WINDOWS_MAX * 4;
 }
 
-bool chunk_order_on(int64_t B) { return B >= CHUNK_ORDER_MIN_B; }
+// ordering needs at least one window per table within CHUNK_WINDOWS_MAX keys
+bool chunk_order_on(int64_t B, int T) {
+    return B >= CHUNK_ORDER_MIN_B && T >= 1 && T <= CHUNK_WINDOWS_MAX;
+}
 
-// windows of 2^shift bags (at least 512) with T * windows <= CHUNK_WINDOWS_MAX
+// windows of 2^shift bags (at least 512) with T * windows <= CHUNK_WINDOWS_MAX;
+// with T <= CHUNK_WINDOWS_MAX the loop ends by the time one window covers B
 int chunk_window_shift(int64_t B, int T) {
     int s = 9;
-    while ((int64_t)T * ((B + (int64_t(1) << s) - 1) >> s) > CHUNK_WINDOWS_MAX) ++s;
+    while (s < 62 && (int64_t)T * ((B + (int64_t(1) << s) - 1) >> s) > CHUNK_WINDOWS_MAX) ++s;
     return s;
 }
 
@@ -263,7 +267,7 @@ tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     const int64_t ntiles = (a.N + RLE_TILE - 1) / RLE_TILE;
     int32_t *tile_heads = (int32_t *)ws;
     int32_t *win = (int32_t *)((char *)ws + ((size_t)(ntiles + 1) * 4 + 255) / 256 * 256);
-    const bool order = chunk_order_on(a.B);
+    const bool order = chunk_order_on(a.B, a.T);
     const int wshift = order ? chunk_window_shift(a.B, a.T) : -1;
     const int nwin = order ? a.T * (int)((a.B + (int64_t(1) << wshift) - 1) >> wshift) : 0;
     L.before("tbe_rle_count");

@@ -146,13 +146,14 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
 size_t rle_workspace_bytes(int64_t N);
 // Long-run chunk slots are taken in order of (table, batch window of 2^wshift
 // bags of their first lookup) when the batch has at least CHUNK_ORDER_MIN_B
-// bags per table, so that concurrently reduced chunks share gradient rows.
+// bags per table and at most CHUNK_WINDOWS_MAX tables, so that concurrently
+// reduced chunks share gradient rows.
 #ifndef TBE_CHUNK_ORDER_MIN_B
 #define TBE_CHUNK_ORDER_MIN_B 4096
 #endif
 constexpr int64_t CHUNK_ORDER_MIN_B = TBE_CHUNK_ORDER_MIN_B;
 constexpr int CHUNK_WINDOWS_MAX = 4096;
-bool chunk_order_on(int64_t B);
+bool chunk_order_on(int64_t B, int T);
 int chunk_window_shift(int64_t B, int T);
 
 struct RleArgs {
