@@ -21,8 +21,9 @@
  *
  * Conventions for every entry point
  *  - Ownership: the caller allocates and owns every buffer.  The library
- *    allocates nothing, frees nothing and keeps no global state; all
- *    scratch memory comes from the caller's `workspace`.
+ *    allocates nothing and frees nothing; all scratch memory comes from the
+ *    caller's `workspace`.  The one exception is tbe_preprocess_static,
+ *    whose scratch is a device array inside the library (see there).
  *  - Pointers named device are device memory; those named host are host
  *    memory read synchronously during the call.
  *  - Streams: every device operation is enqueued on `stream`; the calls
