@@ -193,6 +193,12 @@ void tbe_config_default(tbe_config *cfg);
 tbe_status tbe_query_sizes(const tbe_tables *tables, const tbe_batch *batch,
                            const tbe_config *cfg, size_t *meta_bytes, size_t *workspace_bytes);
 
+/* The two sizes of tbe_query_sizes one at a time (host only): bytes of the
+ * meta buffer and of the workspace, or 0 when the problem is rejected (the
+ * status then comes from tbe_query_sizes). */
+size_t tbe_workspace_bytes(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);
+size_t tbe_meta_bytes(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);
+
 /* Carve `meta` out of device_buf (>= meta_bytes, 256-byte aligned).  Host only. */
 tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes,
                          const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);
@@ -276,6 +282,7 @@ int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const 
 
 /* Static string naming a status code. */
 const char *tbe_status_string(tbe_status status);
+const char *tbe_status_str(tbe_status status);   /* the same text */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t tbe_version(void);

@@ -255,6 +255,16 @@ tbe_status tbe_query_sizes(const tbe_tables *tables, const tbe_batch *batch, con
     return TBE_OK;
 }
 
+size_t tbe_workspace_bytes(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg) {
+    size_t w = 0;
+    return tbe_query_sizes(tables, batch, cfg, nullptr, &w) == TBE_OK ? w : 0;
+}
+
+size_t tbe_meta_bytes(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg) {
+    size_t m = 0;
+    return tbe_query_sizes(tables, batch, cfg, &m, nullptr) == TBE_OK ? m : 0;
+}
+
 int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg) {
     Problem pr;
     if (check_problem(tables, batch, cfg, &pr) != TBE_OK) return 0;
@@ -383,6 +393,8 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
     a.long_mode = pr.long_mode;
     return finish(L, launch_backward(L, a));
 }
+
+const char *tbe_status_str(tbe_status s) { return tbe_status_string(s); }
 
 const char *tbe_status_string(tbe_status s) {
     switch (s) {

@@ -33,7 +33,8 @@ _TORCH_DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTED = ("tbe_config_default", "tbe_query_sizes", "tbe_meta_bind", "tbe_forward",
             "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_select_path",
-            "tbe_status_string", "tbe_version", "tbe_preprocess_static")
+            "tbe_status_string", "tbe_status_str", "tbe_version", "tbe_preprocess_static",
+            "tbe_workspace_bytes", "tbe_meta_bytes")
 STATIC_SCRATCH_MAX_N = 1 << 22
 
 
@@ -102,6 +103,10 @@ def lib():
         L.tbe_status_string.argtypes = [i32]
         L.tbe_version.restype = i32
         L.tbe_version.argtypes = []
+        L.tbe_status_str.restype = ctypes.c_char_p
+        L.tbe_status_str.argtypes = [i32]
+        L.tbe_workspace_bytes.restype = ctypes.c_size_t
+        L.tbe_meta_bytes.restype = ctypes.c_size_t
         _lib = L
     return _lib
 

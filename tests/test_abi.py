@@ -60,6 +60,12 @@ def test_query_sizes_and_meta_bind_layout():
     f = Fake(N=10000, B=100)
     st, mb, wb = f.sizes()
     assert st == 0 and mb >= 6 * 4 * 10000 and wb > 0
+    L0 = f.tbe.lib()
+    assert L0.tbe_meta_bytes(ctypes.byref(f.tab), ctypes.byref(f.bt), None) == mb
+    assert L0.tbe_workspace_bytes(ctypes.byref(f.tab), ctypes.byref(f.bt), None) == wb
+    bad = Fake(D=6)
+    assert L0.tbe_workspace_bytes(ctypes.byref(bad.tab), ctypes.byref(bad.bt), None) == 0
+    assert L0.tbe_status_str(3) == L0.tbe_status_string(3) == b"unsupported embedding dimension"
     m = f.tbe.tbe_meta()
     L = f.tbe.lib()
     assert L.tbe_meta_bind(ctypes.byref(m), FAKE, mb - 1, ctypes.byref(f.tab), ctypes.byref(f.bt), None) == 7
