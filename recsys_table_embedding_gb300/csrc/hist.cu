@@ -8,8 +8,9 @@
 // 64 <= D <= 128, L >= 64, FP16 weights and no per-sample weights.
 //
 // Forward (per CTA: a contiguous range of 128-bag tiles of the tables):
-//   the tile's lookups, one contiguous CSR range, are streamed by all threads
-//   and counted into shared memory (H[b][e], b < 128, e < 64), the counts are
+//   the tile's lookups, one contiguous CSR range, are read warp by warp (a
+//   warp takes 4 bags at a time, its lanes consecutive lookups of each) and
+//   counted into shared memory (H[b][e], b < 128, e < 64), the counts are
 //   written to the A operand as FP16 (exact: counts <= 2048) in the 128-byte
 //   swizzled K-major layout and saved to global memory, and one tcgen05.mma
 //   chain (M = 128 bags, N = D, K = 64 rows, FP32 accumulation in TMEM)
@@ -226,29 +227,44 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
             if (tid <= HT_BAGS) S.offs[tid] = 0;   // treat the tile's bags as empty
             __syncthreads();
         }
-        // stream the tile's lookups (one contiguous range) and count them
-        const int32_t pbeg = S.offs[0], pend = S.offs[nb];
-        for (int32_t base = pbeg; base < pend; base += HF_THREADS * 4) {
-            int32_t idx[4];
+        // count the tile's lookups: a warp takes CB bags at a time and its
+        // lanes read CU*32 consecutive lookups of each (CB*CU loads in flight
+        // per lane); every lookup adds one to its bag's 16-bit row counter
+        {
+            constexpr int CB = 4, CU = 1;
+            constexpr int NW = HF_THREADS / 32;
+            for (int r0 = warp * CB; r0 < nb; r0 += NW * CB) {
+                int32_t bs[CB], be[CB];
+                int32_t maxlen = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int32_t pos = base + u * HF_THREADS + tid;
-                idx[u] = pos < pend ? __ldg(p.indices + pos) : -1;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int32_t pos = base + u * HF_THREADS + tid;
-                if (pos >= pend) continue;
-                // bag of pos: last j with offs[j] <= pos
-                int lo = 0, hi = nb;
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (S.offs[mid] <= pos) lo = mid; else hi = mid;
+                for (int j = 0; j < CB; ++j) {
+                    const int r = r0 + j;
+                    bs[j] = r < nb ? S.offs[r] : 0;
+                    be[j] = r < nb ? S.offs[r + 1] : 0;
+                    maxlen = max(maxlen, be[j] - bs[j]);
                 }
-                if (idx[u] >= 0 && (int64_t)idx[u] < E)
-                    atomicAdd(&S.cnt[lo * CNT_STRIDE + (idx[u] >> 1)], 1u << ((idx[u] & 1) * 16));
-                else
-                    ++oob;
+                for (int32_t k = 0; k < maxlen; k += 32 * CU) {
+                    int32_t v[CB][CU];
+#pragma unroll
+                    for (int j = 0; j < CB; ++j)
+#pragma unroll
+                        for (int u = 0; u < CU; ++u) {
+                            const int32_t pos = bs[j] + k + u * 32 + lane;
+                            v[j][u] = pos < be[j] ? __ldg(p.indices + pos) : 0;
+                        }
+#pragma unroll
+                    for (int j = 0; j < CB; ++j)
+#pragma unroll
+                        for (int u = 0; u < CU; ++u) {
+                            const int32_t pos = bs[j] + k + u * 32 + lane;
+                            if (pos >= be[j]) continue;
+                            const int32_t idx = v[j][u];
+                            if (idx >= 0 && (int64_t)idx < E)
+                                atomicAdd(&S.cnt[(r0 + j) * CNT_STRIDE + (idx >> 1)], 1u << ((idx & 1) * 16));
+                            else
+                                ++oob;
+                        }
+                }
             }
         }
         __syncthreads();
