@@ -588,7 +588,8 @@ def cpu_baseline(workload: str):
             ctx = mp.get_context("spawn")
             jobs = [_table_slice(sub, W, G, j) for j in range(nproc)]
             with ctx.Pool(nproc, initializer=_oracle_worker_init, initargs=(ctx.Barrier(nproc),)) as pool:
-                out = pool.map(_oracle_table_job, jobs, chunksize=1)
+                # bounded: a worker that dies would otherwise leave map() waiting forever
+                out = pool.map_async(_oracle_table_job, jobs, chunksize=1).get(timeout=600)
             n = sum(o[0] for o in out)
             dta = max(o[2] for o in out) - min(o[1] for o in out)
             res["all_cores"] = {"value": round(n / dta, 1), "cores": nproc, "seconds": round(dta, 2),
