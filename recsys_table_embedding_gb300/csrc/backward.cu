@@ -15,15 +15,23 @@
 // section 4: the optimizer update is fused into the backward (one read and
 // one write of each touched row).
 //
-// Design: the owner of a run or chunk is one warp.  Gradient rows are float32
-// [B, T*D]; a row is read as float4 vectors by LPR lanes (NV each), 32/LPR rows
-// per step and U steps in flight.  Partials of chunk slot c live at
-// partials[c*D ...] in the accumulator type.  The long-run sum always adds
-// the chunk partials in chunk order c = 0..k-1, so the two-kernel and the
-// fused modes give bit-identical weights and momentum.  The fused mode needs
-// no waiting: each chunk stores its partial, fences, and bumps the run's
-// arrival counter; only the warp that sees k-1 reads the partials (through
-// L2) and applies, then re-arms the counter.
+// Design.  Gradient rows are float32 [B, T*D].
+//   * Long runs: a warp per 256-lookup chunk, chunks taken in (table, bag
+//     window) order; rows arrive through a per-warp ring of bulk copies
+//     (cp.async.bulk into shared memory, mbarrier completion) that streams
+//     across chunk boundaries.  Partials of chunk slot c live at
+//     partials[c*D ...] in the accumulator type.  The long-run sum always
+//     adds the chunk partials in chunk order c = 0..k-1, so the two-kernel
+//     and the fused modes give bit-identical weights and momentum.  The fused
+//     mode needs no waiting: each chunk stores its partial, fences, and bumps
+//     the run's arrival counter; only the warp that sees k-1 reads the
+//     partials (through L2) and applies, then re-arms the counter.
+//   * Short runs, unweighted batches (and rows under 512 bytes): a group of
+//     lanes per run reads rows as float4 vectors from global memory, with the
+//     weight slice and momentum loaded ahead.
+//   * Short runs, weighted batches with rows of 512 bytes and more: a warp
+//     streams the rows of consecutive runs through a bulk-copy ring and
+//     applies each run's update from weight rows prefetched per task.
 #include "tbe_internal.cuh"
 
 namespace tbe {
