@@ -44,17 +44,19 @@ def lib():
         i32, i64, f32, f64, u16 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                    ctypes.c_double, ctypes.c_uint16)
         L.tbe_oracle_forward.restype = i64
-        L.tbe_oracle_forward.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P]
+        L.tbe_oracle_forward.argtypes = [i32, i64, i32, i32, P, P, P, P, i64, P, P, P, i64, P, P, P]
         L.tbe_oracle_preprocess.restype = i64
         L.tbe_oracle_preprocess.argtypes = [i32, i64, P, P, P, i64, P, P, P, P, P, P]
         L.tbe_oracle_backward_adagrad.restype = i64
         L.tbe_oracle_backward_adagrad.argtypes = [i32, i64, i32, i32, P, P, P, P, P, i64, P, P, P,
-                                                  f32, f32, P, P]
+                                                  f32, f32, P, P, P]
         L.tbe_oracle_rows_update.restype = i64
-        L.tbe_oracle_rows_update.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, f32, f32, P, i64,
-                                             P, P, P, P]
+        L.tbe_oracle_rows_update.argtypes = [i32, i64, i32, i32, P, P, P, i64, P, P, P, f32, f32, P,
+                                             i64, P, P, P, P, P]
         L.tbe_oracle_histogram.restype = i64
-        L.tbe_oracle_histogram.argtypes = [i32, i64, i32, P, P, P, P]
+        L.tbe_oracle_histogram.argtypes = [i32, i64, i32, P, P, P, i64, P]
+        L.tbe_oracle_offsets_check.restype = i32
+        L.tbe_oracle_offsets_check.argtypes = [i32, i64, P, i64, P, P, P]
         for n in ("tbe_oracle_to_half", "tbe_oracle_to_bf16"):
             getattr(L, n).restype = u16
             getattr(L, n).argtypes = [f64]
@@ -90,8 +92,8 @@ def forward(wl, W: np.ndarray, bags: Optional[np.ndarray] = None, want_abs: bool
     L = lib()
     W = _wbits(W, wl.dtype)
     to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
-    idx = _c(wl.indices, np.int32)
-    off = _c(wl.offsets, np.int32)
+    idx = _c(wl.indices, np.int64)
+    off = _c(wl.offsets, np.int64)
     psw = _c(wl.per_sample_weights, np.float32)
     wt = _c(wl.weighted_tables, np.uint8)
     if bags is None:
@@ -104,7 +106,7 @@ def forward(wl, W: np.ndarray, bags: Optional[np.ndarray] = None, want_abs: bool
     ab = np.zeros(out.shape, dtype=np.float64) if want_abs else None
     bad = ctypes.c_int64(0)
     oob = L.tbe_oracle_forward(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(to), _p(idx),
-                               _p(off), _p(psw), _p(wt), _p(bags), nb, _p(out), _p(ab),
+                               _p(off), wl.N, _p(psw), _p(wt), _p(bags), nb, _p(out), _p(ab),
                                ctypes.addressof(bad))
     return out, ab, int(oob), int(bad.value)
 
@@ -121,19 +123,22 @@ def preprocess(wl):
     rl = np.zeros(max(N, 1), np.int64)
     so = np.zeros(N + 1, np.int64)
     nv = ctypes.c_int64(0)
-    U = L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(_c(wl.indices, np.int32)),
-                                _p(_c(wl.offsets, np.int32)), N, _p(sk), _p(sp), _p(uk), _p(rl),
-                                _p(so), ctypes.addressof(nv))
+    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
+    U = L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(idx), _p(off), N, _p(sk), _p(sp), _p(uk),
+                                _p(rl), _p(so), ctypes.addressof(nv))
     nv = int(nv.value)
     return dict(sorted_keys=sk[:nv], sorted_pos=sp[:nv], unique_keys=uk[:U], run_len=rl[:U],
                 seg_off=so[:U + 1], num_unique=int(U), n_valid=nv)
 
 
 def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarray,
-                     want_row_grad: bool = False, want_update_count: bool = False):
+                     want_row_grad: bool = False, want_update_count: bool = False,
+                     want_row_abs: bool = False):
     """Backward + exact rowwise Adagrad, in place on copies.
 
-    Returns (W_new, momentum_new, U, row_grad|None, update_count|None).
+    Returns (W_new, momentum_new, U, row_grad|None, update_count|None), plus
+    row_abs (the per-element sum of the row gradient's term magnitudes) as a
+    sixth item when ``want_row_abs``.
     """
     L = lib()
     W = _wbits(W, wl.dtype).copy()
@@ -141,19 +146,24 @@ def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarr
     to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
     go = np.ascontiguousarray(grad_out, dtype=np.float32)
     rg = np.zeros((wl.rows_total, wl.D), np.float64) if want_row_grad else None
+    ra = np.zeros((wl.rows_total, wl.D), np.float64) if want_row_abs else None
     uc = np.zeros(wl.rows_total, np.int32) if want_update_count else None
+    # widened copies are held in locals: the C call reads them
+    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
+    psw, wt = _c(wl.per_sample_weights, np.float32), _c(wl.weighted_tables, np.uint8)
     U = L.tbe_oracle_backward_adagrad(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(m), _p(to),
-                                      _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)),
-                                      wl.N, _p(_c(wl.per_sample_weights, np.float32)),
-                                      _p(_c(wl.weighted_tables, np.uint8)), _p(go),
-                                      float(wl.lr), float(wl.eps), _p(rg), _p(uc))
+                                      _p(idx), _p(off), wl.N, _p(psw), _p(wt), _p(go),
+                                      float(wl.lr), float(wl.eps), _p(rg), _p(ra), _p(uc))
+    if want_row_abs:
+        return W, m, int(U), rg, uc, ra
     return W, m, int(U), rg, uc
 
 
 def rows_update(wl, rows: np.ndarray, W_rows: np.ndarray, mom_rows: np.ndarray,
-                grad_out: np.ndarray):
+                grad_out: np.ndarray, want_row_abs: bool = False):
     """Sampled-row backward: rows (sorted distinct linearised keys) with their
-    pre-update W rows and momentum.  Returns (W_rows_new, mom_new, row_grad, counts, n_valid)."""
+    pre-update W rows and momentum.  Returns (W_rows_new, mom_new, row_grad,
+    counts, n_valid), plus row_abs as a sixth item when ``want_row_abs``."""
     L = lib()
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     assert np.all(np.diff(rows) > 0)
@@ -161,15 +171,17 @@ def rows_update(wl, rows: np.ndarray, W_rows: np.ndarray, mom_rows: np.ndarray,
     Wr = _wbits(W_rows, wl.dtype).copy()
     mr = np.ascontiguousarray(mom_rows, dtype=np.float32).copy()
     rg = np.zeros((k, wl.D), np.float64)
+    ra = np.zeros((k, wl.D), np.float64) if want_row_abs else None
     cnt = np.zeros(k, np.int64)
     to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
-    nv = L.tbe_oracle_rows_update(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(to),
-                                  _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)),
-                                  _p(_c(wl.per_sample_weights, np.float32)),
-                                  _p(_c(wl.weighted_tables, np.uint8)),
-                                  _p(np.ascontiguousarray(grad_out, dtype=np.float32)),
-                                  float(wl.lr), float(wl.eps), _p(rows), k, _p(Wr), _p(mr),
-                                  _p(rg), _p(cnt))
+    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
+    psw, wt = _c(wl.per_sample_weights, np.float32), _c(wl.weighted_tables, np.uint8)
+    go = np.ascontiguousarray(grad_out, dtype=np.float32)
+    nv = L.tbe_oracle_rows_update(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(to), _p(idx), _p(off),
+                                  wl.N, _p(psw), _p(wt), _p(go), float(wl.lr), float(wl.eps),
+                                  _p(rows), k, _p(Wr), _p(mr), _p(rg), _p(ra), _p(cnt))
+    if want_row_abs:
+        return Wr, mr, rg, cnt, int(nv), ra
     return Wr, mr, rg, cnt, int(nv)
 
 
@@ -177,9 +189,24 @@ def histogram(wl, Emax: int = 64) -> np.ndarray:
     """Per-bag row counts, int32 [T, B, Emax]."""
     L = lib()
     c = np.zeros((wl.T, wl.B, Emax), np.int32)
-    L.tbe_oracle_histogram(wl.T, wl.B, Emax, _p(np.ascontiguousarray(wl.table_offset, np.int64)),
-                           _p(_c(wl.indices, np.int32)), _p(_c(wl.offsets, np.int32)), _p(c))
+    to = np.ascontiguousarray(wl.table_offset, np.int64)
+    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
+    L.tbe_oracle_histogram(wl.T, wl.B, Emax, _p(to), _p(idx), _p(off), wl.N, _p(c))
     return c
+
+
+def offsets_check(wl):
+    """(malformed, bad_bags, decreasing, span) of the batch's offsets: bags
+    not 0 <= start <= end <= N, whether any bag has end < start, whether
+    offsets[0] != 0 or offsets[T*B] != N."""
+    L = lib()
+    bad = ctypes.c_int64(0)
+    dec = ctypes.c_int32(0)
+    sp = ctypes.c_int32(0)
+    off = _c(wl.offsets, np.int64)
+    m = L.tbe_oracle_offsets_check(wl.T, wl.B, _p(off), wl.N,
+                                   ctypes.addressof(bad), ctypes.addressof(dec), ctypes.addressof(sp))
+    return bool(m), int(bad.value), bool(dec.value), bool(sp.value)
 
 
 def to_half_bits(x: float) -> int:

@@ -43,8 +43,19 @@
  * accurate as either, so a comparison measures the kernel's own rounding.
  *
  * Out-of-range indices (idx < 0 or idx >= E_t) are counted, contribute
- * nothing to the forward and take no part in the backward.  A bag whose end
- * offset is below its start is counted as malformed and treated as empty.
+ * nothing to the forward and take no part in the backward.
+ *
+ * Malformed offsets (the pages say nothing about them; this is the reading
+ * both sides implement):
+ *  - a bag (t,b) is well formed when 0 <= offsets[g] <= offsets[g+1] <= N
+ *    (g = t*B + b); any other bag is malformed, counted, and empty;
+ *  - lookups outside every well-formed bag (before offsets[0], after
+ *    offsets[T*B], or inside a malformed bag) take no part in the forward or
+ *    the backward;
+ *  - offsets that decrease anywhere (some bag with end < start) leave no
+ *    single bag for a lookup that two well-formed bags both cover, so such a
+ *    batch gets no backward update at all (its forward still pools each
+ *    well-formed bag over its own range).
  *
  * Dtype codes: 0 = float32, 1 = float16, 2 = bfloat16.
  */
@@ -171,18 +182,19 @@ static double sample_weight(const float *psw, const uint8_t *weighted, int64_t t
  *
  *   out[b, t*D + d] = sum_{p in bag (t,b), 0 <= idx_p < E_t} w_p * W[table_offset[t] + idx_p, d]
  *
- * With bags == NULL the output is the full [B, T*D] matrix; with a bag list
- * row k of out ([nbags, D]) belongs to bag bags[k] = t*B + b.
+ * indices[N] and offsets[T*B+1] are int64 here (the caller widens int32
+ * inputs).  With bags == NULL the output is the full [B, T*D] matrix; with a
+ * bag list row k of out ([nbags, D]) belongs to bag bags[k] = t*B + b.
  * abs_sum (nullable) receives sum |w_p * W[.., d]| in the same layout: the
  * scale that bounds any summation-order rounding of out.
  * Returns the number of out-of-range lookups in the bags visited;
- * *bad_bags (nullable) the number of bags with end < start.
+ * *bad_bags (nullable) the number of malformed bags among them.
  */
 int64_t tbe_oracle_forward(int32_t T, int64_t B, int32_t D, int32_t dtype, const void *W,
-                           const int64_t *table_offset, const int32_t *indices,
-                           const int32_t *offsets, const float *psw, const uint8_t *weighted,
-                           const int64_t *bags, int64_t nbags, float *out, double *abs_sum,
-                           int64_t *bad_bags)
+                           const int64_t *table_offset, const int64_t *indices,
+                           const int64_t *offsets, int64_t N, const float *psw,
+                           const uint8_t *weighted, const int64_t *bags, int64_t nbags,
+                           float *out, double *abs_sum, int64_t *bad_bags)
 {
     int64_t oob = 0, bad = 0;
     int64_t n = bags ? nbags : (int64_t)T * B;
@@ -195,8 +207,10 @@ int64_t tbe_oracle_forward(int32_t T, int64_t B, int32_t D, int32_t dtype, const
         for (int d = 0; d < D; ++d)
             acc[d] = aab[d] = 0.0;
         int64_t start = offsets[bag], end = offsets[bag + 1];
-        if (end < start)
-            ++bad;
+        if (!(0 <= start && start <= end && end <= N)) {
+            ++bad;                       /* malformed bag: empty */
+            start = end = 0;
+        }
         for (int64_t p = start; p < end; ++p) {
             int64_t idx = indices[p];
             if (idx < 0 || idx >= E) {
@@ -243,21 +257,61 @@ static int cmp_key_pos(const void *a, const void *b)
     return 0;
 }
 
-/* bag id (t*B + b) of every position p; -1 for positions in no bag */
-static int64_t *bag_of_positions(int32_t T, int64_t B, const int32_t *offsets, int64_t N)
+/*
+ * Shape of the offsets array: *bad_bags = malformed bags (not
+ * 0 <= offsets[g] <= offsets[g+1] <= N), *decreasing = 1 when some bag has
+ * end < start, *span = 1 when offsets[0] != 0 or offsets[T*B] != N.
+ * Returns 1 when any of the three holds (the batch's offsets are malformed).
+ */
+int32_t tbe_oracle_offsets_check(int32_t T, int64_t B, const int64_t *offsets, int64_t N,
+                                 int64_t *bad_bags, int32_t *decreasing, int32_t *span)
+{
+    int64_t NB = (int64_t)T * B, bad = 0;
+    int32_t dec = 0;
+    for (int64_t g = 0; g < NB; ++g) {
+        int64_t s = offsets[g], e = offsets[g + 1];
+        if (e < s)
+            dec = 1;
+        if (!(0 <= s && s <= e && e <= N))
+            ++bad;
+    }
+    int32_t sp = offsets[0] != 0 || offsets[NB] != N;
+    if (bad_bags)
+        *bad_bags = bad;
+    if (decreasing)
+        *decreasing = dec;
+    if (span)
+        *span = sp;
+    return bad > 0 || dec || sp;
+}
+
+/*
+ * Bag id (t*B + b) of every position p for the backward; -1 for positions in
+ * no well-formed bag.  Offsets that decrease anywhere give -1 everywhere
+ * (such a batch has no backward update).
+ */
+static int64_t *bag_of_positions(int32_t T, int64_t B, const int64_t *offsets, int64_t N)
 {
     int64_t *bag = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     for (int64_t p = 0; p < N; ++p)
         bag[p] = -1;
-    for (int64_t g = 0; g < (int64_t)T * B; ++g)
-        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p)
-            if (p >= 0 && p < N)
-                bag[p] = g;
+    int32_t dec = 0;
+    tbe_oracle_offsets_check(T, B, offsets, N, NULL, &dec, NULL);
+    if (dec)
+        return bag;
+    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
+        int64_t s = offsets[g], e = offsets[g + 1];
+        if (!(0 <= s && s <= e && e <= N))
+            continue;
+        for (int64_t p = s; p < e; ++p)
+            bag[p] = g;
+    }
     return bag;
 }
 
 /*
- * key_p = table_offset[t] + idx_p for every in-range lookup p (t its table),
+ * key_p = table_offset[t] + idx_p for every in-range lookup p of a
+ * well-formed bag (t its table; see bag_of_positions),
  * sorted by (key, p) -- a stable sort by key -- then run-length encoded:
  *   unique_keys[r], run_len[r], seg_off[r] (exclusive prefix sum of run_len,
  *   seg_off[U] = N' = number of in-range lookups).
@@ -265,7 +319,7 @@ static int64_t *bag_of_positions(int32_t T, int64_t B, const int32_t *offsets, i
  * Returns U.
  */
 int64_t tbe_oracle_preprocess(int32_t T, int64_t B, const int64_t *table_offset,
-                              const int32_t *indices, const int32_t *offsets, int64_t N,
+                              const int64_t *indices, const int64_t *offsets, int64_t N,
                               int64_t *sorted_keys, int64_t *sorted_pos, int64_t *unique_keys,
                               int64_t *run_len, int64_t *seg_off, int64_t *n_valid)
 {
@@ -335,15 +389,17 @@ static void adagrad_row(void *W, float *momentum, int32_t D, int32_t dtype, int6
  * and exactly one Adagrad update of that row.  W and momentum are updated in
  * place; rows no in-range lookup touches are not written.
  * row_grad (nullable, [rows_total, D]) receives g of every touched row;
+ * row_abs (nullable, [rows_total, D]) receives sum |w_p * grad_out[..]| of
+ * the same terms (the scale that bounds a summation-order rounding of g);
  * update_count (nullable, [rows_total]) counts updates applied per row.
  * Returns U, the number of rows updated.
  */
 int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dtype, void *W,
                                     float *momentum, const int64_t *table_offset,
-                                    const int32_t *indices, const int32_t *offsets, int64_t N,
+                                    const int64_t *indices, const int64_t *offsets, int64_t N,
                                     const float *psw, const uint8_t *weighted,
                                     const float *grad_out, float lr, float eps,
-                                    double *row_grad, int32_t *update_count)
+                                    double *row_grad, double *row_abs, int32_t *update_count)
 {
     int64_t *skeys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     int64_t *spos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
@@ -353,26 +409,33 @@ int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dty
                                       NULL, soff, NULL);
     int64_t *bag = bag_of_positions(T, B, offsets, N);
     double *g = (double *)malloc(sizeof(double) * (size_t)D);
+    double *ga = (double *)malloc(sizeof(double) * (size_t)D);
     for (int64_t r = 0; r < U; ++r) {
         int64_t row = ukeys[r];
         for (int d = 0; d < D; ++d)
-            g[d] = 0.0;
+            g[d] = ga[d] = 0.0;
         for (int64_t i = soff[r]; i < soff[r + 1]; ++i) {
             int64_t p = spos[i];
             int64_t t = bag[p] / B, b = bag[p] % B;
             double w = sample_weight(psw, weighted, t, p);
             const float *grow = grad_out + (b * T + t) * D;
-            for (int d = 0; d < D; ++d)
+            for (int d = 0; d < D; ++d) {
                 g[d] += w * (double)grow[d];
+                ga[d] += fabs(w * (double)grow[d]);
+            }
         }
         if (row_grad)
             for (int d = 0; d < D; ++d)
                 row_grad[row * D + d] = g[d];
+        if (row_abs)
+            for (int d = 0; d < D; ++d)
+                row_abs[row * D + d] = ga[d];
         adagrad_row(W, momentum, D, dtype, row, g, lr, eps);
         if (update_count)
             update_count[row] += 1;
     }
     free(g);
+    free(ga);
     free(bag);
     free(soff);
     free(ukeys);
@@ -392,28 +455,40 @@ static int cmp_i64(const void *a, const void *b)
 
 /*
  * For k sampled linearised rows (sorted ascending, distinct) compute by one
- * scan over all lookups their lookup count, row gradient (summed in position
- * order, double) and the Adagrad result.  W_rows (dtype, [k, D]) and
+ * scan over all lookups of the well-formed bags their lookup count, row
+ * gradient (summed in position order, double; row_abs, nullable, the sum of
+ * the terms' magnitudes) and the Adagrad result.  W_rows (dtype, [k, D]) and
  * mom_rows ([k]) hold the rows' values before the update and are updated in
  * place; rows with count 0 are left untouched.  row_grad ([k, D]) and counts
  * ([k]) are outputs.  Returns the number of in-range lookups scanned.
  */
 int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
-                               const int64_t *table_offset, const int32_t *indices,
-                               const int32_t *offsets, const float *psw, const uint8_t *weighted,
-                               const float *grad_out, float lr, float eps, const int64_t *rows,
-                               int64_t k, void *W_rows, float *mom_rows, double *row_grad,
+                               const int64_t *table_offset, const int64_t *indices,
+                               const int64_t *offsets, int64_t N, const float *psw,
+                               const uint8_t *weighted, const float *grad_out, float lr,
+                               float eps, const int64_t *rows, int64_t k, void *W_rows,
+                               float *mom_rows, double *row_grad, double *row_abs,
                                int64_t *counts)
 {
     int64_t nv = 0;
-    for (int64_t i = 0; i < k * D; ++i)
+    for (int64_t i = 0; i < k * D; ++i) {
         row_grad[i] = 0.0;
+        if (row_abs)
+            row_abs[i] = 0.0;
+    }
     for (int64_t i = 0; i < k; ++i)
         counts[i] = 0;
+    int32_t dec = 0;
+    tbe_oracle_offsets_check(T, B, offsets, N, NULL, &dec, NULL);
+    if (dec)
+        return 0;                        /* decreasing offsets: no update */
     for (int64_t g = 0; g < (int64_t)T * B; ++g) {
         int64_t t = g / B, b = g % B;
         int64_t E = table_offset[t + 1] - table_offset[t];
-        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
+        int64_t s = offsets[g], e = offsets[g + 1];
+        if (!(0 <= s && s <= e && e <= N))
+            continue;                    /* malformed bag */
+        for (int64_t p = s; p < e; ++p) {
             int64_t idx = indices[p];
             if (idx < 0 || idx >= E)
                 continue;
@@ -422,12 +497,15 @@ int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
             const int64_t *hit = (const int64_t *)bsearch(&key, rows, (size_t)k, sizeof(int64_t), cmp_i64);
             if (!hit)
                 continue;
-            int64_t s = hit - rows;
+            int64_t r = hit - rows;
             double w = sample_weight(psw, weighted, t, p);
             const float *grow = grad_out + (b * T + t) * D;
-            for (int d = 0; d < D; ++d)
-                row_grad[s * D + d] += w * (double)grow[d];
-            counts[s] += 1;
+            for (int d = 0; d < D; ++d) {
+                row_grad[r * D + d] += w * (double)grow[d];
+                if (row_abs)
+                    row_abs[r * D + d] += fabs(w * (double)grow[d]);
+            }
+            counts[r] += 1;
         }
     }
     for (int64_t s = 0; s < k; ++s)
@@ -441,18 +519,24 @@ int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
 
 /*
  * counts[(t*B + b)*Emax + e] = #{p in bag (t,b) : idx_p == e}, for
- * 0 <= e < E_t (out-of-range lookups are not counted).  Emax >= every E_t.
+ * 0 <= e < E_t (out-of-range lookups and malformed bags are not counted).
+ * Emax >= every E_t.  These are the forward's counts: a lookup that two
+ * well-formed bags cover counts in both.
  * Returns the number of lookups counted.
  */
 int64_t tbe_oracle_histogram(int32_t T, int64_t B, int32_t Emax, const int64_t *table_offset,
-                             const int32_t *indices, const int32_t *offsets, int32_t *counts)
+                             const int64_t *indices, const int64_t *offsets, int64_t N,
+                             int32_t *counts)
 {
     int64_t total = 0;
     memset(counts, 0, sizeof(int32_t) * (size_t)T * (size_t)B * (size_t)Emax);
     for (int64_t g = 0; g < (int64_t)T * B; ++g) {
         int64_t t = g / B;
         int64_t E = table_offset[t + 1] - table_offset[t];
-        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
+        int64_t s = offsets[g], e = offsets[g + 1];
+        if (!(0 <= s && s <= e && e <= N))
+            continue;                    /* malformed bag: empty */
+        for (int64_t p = s; p < e; ++p) {
             int64_t idx = indices[p];
             if (idx < 0 || idx >= E)
                 continue;

@@ -272,23 +272,27 @@ def test_each_touched_row_updated_once_untouched_rows_identical(dtype):
     assert np.all(m[touched] >= m0[touched])
 
 
-def _closed_form_workload(dtype, c, steps=1):
+def _closed_form_workload(dtype, c, eps=1e-8):
     """One table of 6 rows; bag b looks up row b once (rows 4, 5 untouched);
     every upstream gradient element is c, so each touched row has g[d] = c."""
     wl = workloads.Workload(name="cf", T=1, B=4, D=8, dtype=dtype, table_rows=np.array([6]),
                             offsets=np.arange(5, dtype=np.int32),
                             indices=np.arange(4, dtype=np.int32), per_sample_weights=None,
-                            weighted_tables=None, lr=0.01, eps=1e-8)
+                            weighted_tables=None, lr=0.01, eps=eps)
     G = np.full((4, 8), c, np.float32)
     return wl, G
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("c", [0.5, -2.0])
-def test_adagrad_closed_form_constant_gradient(dtype, c):
+@pytest.mark.parametrize("c,eps", [(0.5, 1e-8), (-2.0, 1e-8), (0.5, 0.5), (-0.25, 2.0)])
+def test_adagrad_closed_form_constant_gradient(dtype, c, eps):
     # momentum 0 and g[d] = c for all d:  m = c^2 after one step, and after k
-    # steps m = k c^2 and w_k = w_{k-1} - lr c / (sqrt(k) |c| + eps).
-    wl, G = _closed_form_workload(dtype, c)
+    # steps m = k c^2 and w_k = w_{k-1} - lr c / (sqrt(k) |c| + eps).  With a
+    # large eps (0.5 against |c| = 0.5: 1/(0.5+0.5) = 1 but 1/sqrt(0.25+0.5)
+    # = 1.155) eps inside the square root, or the old momentum in the
+    # denominator, moves every updated weight by far more than one unit of
+    # its type.
+    wl, G = _closed_form_workload(dtype, c, eps)
     W = wl.weights()
     Wb = wbits(wl, W)
     m = wl.momentum()
@@ -346,3 +350,125 @@ def test_large_preset_matches_pages_statistics():
     uniq, hot = workloads.expected_zm_stats(E, B * L, workloads.LARGE_ZM_ALPHA, workloads.LARGE_ZM_Q)
     assert abs(T * uniq - s["unique_indices"]) / s["unique_indices"] < 0.05
     assert abs(hot - s["max_frequency"]) / s["max_frequency"] < 0.05
+
+
+# ---------------------------------------------------------------- malformed offsets
+
+def _sub_batch(wl, offsets, indices, psw=None):
+    return workloads.Workload(name=wl.name, T=wl.T, B=wl.B, D=wl.D, dtype=wl.dtype,
+                              table_rows=wl.table_rows, offsets=np.asarray(offsets, np.int64),
+                              indices=np.asarray(indices, np.int32),
+                              per_sample_weights=None if psw is None else np.asarray(psw, np.float32),
+                              weighted_tables=wl.weighted_tables, lr=wl.lr, eps=wl.eps)
+
+
+def _both_results(wl, W, m0, G):
+    out, _, oob, bad = oracle.forward(wl, W)
+    Wn, m, U, _, _ = oracle.backward_adagrad(wl, W, m0, G)
+    return out, Wn, m, U
+
+
+def _junk(rng, n, E=7):
+    # in-range and out-of-range values alike: any of them counted would show
+    return rng.integers(-3, E + 3, size=n).astype(np.int32)
+
+
+def test_lookups_outside_every_bag_take_no_part():
+    # the same bags with junk lookups before offsets[0] and after offsets[T*B]:
+    # forward, weights and momentum equal those of the batch without them
+    wl = small(seed=13, weighted=True, oob=0.03)
+    W = wbits(wl, wl.weights())
+    G = wl.grad_out()
+    m0 = np.random.default_rng(2).uniform(0, 1, wl.rows_total).astype(np.float32)
+    rng = np.random.default_rng(4)
+    pre, post = 5, 7
+    idx = np.concatenate([_junk(rng, pre), wl.indices, _junk(rng, post)])
+    psw = np.concatenate([rng.uniform(0, 1, pre), wl.per_sample_weights, rng.uniform(0, 1, post)])
+    gap = _sub_batch(wl, wl.offsets.astype(np.int64) + pre, idx, psw)
+    a, b = _both_results(wl, W, m0, G), _both_results(gap, W, m0, G)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    assert oracle.offsets_check(gap) == (True, 0, False, True)
+    assert oracle.offsets_check(wl) == (False, 0, False, False)
+
+
+@pytest.mark.parametrize("where", ["first_start_negative", "last_end_past_n", "middle_end_below_start"])
+def test_malformed_bag_is_empty(where):
+    wl = small(seed=17, B=11, rows=(9, 40))
+    W = wbits(wl, wl.weights())
+    G = wl.grad_out()
+    m0 = np.zeros(wl.rows_total, np.float32)
+    off = wl.offsets.astype(np.int64).copy()
+    NB, N = wl.NB, wl.N
+    if where == "first_start_negative":
+        g = 0
+        off[0] = -2
+        # expected: bag 0's lookups gone, everything else as before
+        exp_idx = wl.indices[wl.offsets[1]:]
+        exp_off = np.concatenate([[0], off[1:] - off[1]])
+    elif where == "last_end_past_n":
+        g = NB - 1
+        off[NB] = N + 3
+        exp_idx = wl.indices[:wl.offsets[NB - 1]]
+        exp_off = np.concatenate([off[:NB], [off[NB - 1]]])
+    else:
+        g = 4
+        while off[g] == off[g + 1]:
+            g += 1
+        # bag g ends before its start; bag g+1 starts there and so covers
+        # bag g's lookups too
+        off[g + 1] = off[g] - 1
+        exp_idx = None
+    mal = _sub_batch(wl, off, wl.indices)
+    check = oracle.offsets_check(mal)
+    assert check[0] and check[1] >= 1
+    out, _, _, bad = oracle.forward(mal, W)
+    assert bad == check[1]
+    t, b = divmod(g, wl.B)
+    assert np.all(out[b, t * wl.D:(t + 1) * wl.D] == 0)
+    if exp_idx is not None:
+        assert check[2] is False                     # offsets still non-decreasing
+        exp = _sub_batch(wl, exp_off, exp_idx)
+        a, c = _both_results(mal, W, m0, G), _both_results(exp, W, m0, G)
+        for x, y in zip(a, c):
+            np.testing.assert_array_equal(x, y)
+    else:
+        assert check[2] is True
+        # forward: every well-formed bag pools its own range, as a batch that
+        # holds a private copy of each well-formed bag's lookups does
+        parts, lens = [], []
+        for h in range(NB):
+            s0, e0 = off[h], off[h + 1]
+            ok = 0 <= s0 <= e0 <= N
+            parts.append(wl.indices[s0:e0] if ok else np.zeros(0, np.int32))
+            lens.append(e0 - s0 if ok else 0)
+        copy = _sub_batch(wl, np.concatenate([[0], np.cumsum(lens)]), np.concatenate(parts))
+        np.testing.assert_array_equal(out, oracle.forward(copy, W)[0])
+        # backward: offsets that decrease leave some lookup in two bags, so
+        # the batch updates nothing
+        Wn, m, U, _, _ = oracle.backward_adagrad(mal, W, m0, G)
+        assert U == 0
+        np.testing.assert_array_equal(Wn, W)
+        np.testing.assert_array_equal(m, m0)
+        assert oracle.preprocess(mal)["n_valid"] == 0
+        rows = np.arange(wl.rows_total)
+        _, _, _, cnt, nv = oracle.rows_update(mal, rows, W, m0, G)
+        assert nv == 0 and not cnt.any()
+
+
+def test_offsets_check_patterns():
+    wl = small(seed=19, B=6, rows=(5,))
+    N = wl.N
+    def chk(off):
+        return oracle.offsets_check(_sub_batch(wl, off, wl.indices))
+    base = wl.offsets.astype(np.int64)
+    assert chk(base) == (False, 0, False, False)
+    o = base.copy(); o[-1] = N - 1
+    assert chk(o) == (True, 0, False, True)          # last lookup in no bag
+    o = base.copy(); o[0] = 1
+    assert chk(o)[0] and chk(o)[3]                   # first lookup in no bag
+    o = base.copy(); o[2] = o[1] - 1
+    r = chk(o)
+    assert r[0] and r[1] >= 1 and r[2]               # decreasing
+    o = base.copy(); o[-1] = N + 1
+    assert chk(o) == (True, 1, False, True)          # last bag past N
