@@ -38,6 +38,16 @@
  *        dev_status[1]  |= TBE_FLAG_* bits
  *    The caller zeroes dev_status when it wants a fresh count.  No kernel
  *    traps, asserts or waits without bound.
+ *  - Malformed offsets (the pages do not cover them): a bag (t,b) is well
+ *    formed when 0 <= offsets[g] <= offsets[g+1] <= N (g = t*B+b).  A
+ *    malformed bag is empty (zero output, no part in the backward).
+ *    Lookups outside every well-formed bag (before offsets[0], after
+ *    offsets[T*B], inside a malformed bag) are ignored by forward and
+ *    backward.  When offsets decrease anywhere (a bag with end < start), two
+ *    well-formed bags can both hold a lookup, and the batch gets no backward
+ *    update at all; its forward still pools each well-formed bag over its
+ *    own range.  Any of these, and offsets[0] != 0 or offsets[T*B] != N,
+ *    sets TBE_FLAG_BAD_OFFSETS.
  *  - Threading: the functions are reentrant; calls on different streams
  *    must use different workspace and meta buffers.
  */
@@ -72,7 +82,7 @@ typedef enum tbe_status {
 typedef enum tbe_dtype { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
 
 /* dev_status[1] bits */
-#define TBE_FLAG_BAD_OFFSETS   0x1  /* a bag with offsets[g+1] < offsets[g]; treated as empty */
+#define TBE_FLAG_BAD_OFFSETS   0x1  /* malformed offsets (see the conventions above) */
 #define TBE_FLAG_FP16_OVERFLOW 0x2  /* |grad| > 65504 in the histogram path's FP16 hi/lo split */
 #define TBE_FLAG_SORT_TIMEOUT  0x4  /* radix-sort look-back gave up waiting: sort output invalid */
 #define TBE_FLAG_HIST_COUNT    0x8  /* a histogram count exceeded 2048 (not exact in FP16) */
@@ -276,6 +286,29 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
  */
 tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_batch *batch, tbe_meta *meta,
                                  int32_t *dev_status, const tbe_config *cfg, cudaStream_t stream);
+
+/*
+ * Self-test of the failure detection of device waits (no counterpart on the
+ * pages).  Every device-side wait of this library -- the radix sort's
+ * look-back on earlier tiles, the mbarrier waits of the bulk-copy rings and
+ * of the tensor-core path -- gives up after one second, sets a dev_status[1]
+ * flag and returns, so a wait that can never end costs a second and an error
+ * status instead of a hung GPU.  This call runs one such wait on a condition
+ * that nothing will ever satisfy, so the caller can check that the limit
+ * works and that the context stays usable afterwards:
+ *   TBE_SELFTEST_SORT_LOOKBACK  one radix-sort CTA looks back at a tile that
+ *       no CTA publishes; sets TBE_FLAG_SORT_TIMEOUT.  Needs `workspace`
+ *       (device, 256-byte aligned, >= tbe_selftest_workspace_bytes()).
+ *   TBE_SELFTEST_COPY_WAIT      one warp waits on an mbarrier phase that no
+ *       copy completes; sets TBE_FLAG_COPY_TIMEOUT.  workspace unused.
+ * Nothing is copied while the waits run.  Asynchronous on `stream`; the flag
+ * is visible after the stream completes (about one second later).
+ */
+#define TBE_SELFTEST_SORT_LOOKBACK 0
+#define TBE_SELFTEST_COPY_WAIT 1
+size_t tbe_selftest_workspace_bytes(void);
+tbe_status tbe_selftest_wait_limit(int32_t kind, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, cudaStream_t stream);
 
 /* Which path tbe_forward will take for this problem: 1 generic, 2 histogram. */
 int32_t tbe_select_path(const tbe_tables *tables, const tbe_batch *batch, const tbe_config *cfg);

@@ -223,35 +223,64 @@ __device__ __forceinline__ Chunk load_chunk(const BwdParams &p, int ci) {
     c.slot = slot;
     return c;
 }
-// Exact rowwise Adagrad on row `row` from the reduced gradient in acc:
-//   m += mean_d(g^2);  w -= lr * g / (sqrt(m) + eps)
-// Only lanes of sub-group 0 hold meaningful values; every lane takes part in
-// the shuffles.
+// Exact rowwise Adagrad arithmetic, m += mean_d(g^2); w -= lr*g/(sqrt(m)+eps),
+// in the accumulator's precision: FP64 for FP32 tables, from the FP64 row
+// gradient (decision checklist item 1's FP64 accumulation carried through the
+// update, so the stored weight is the correctly rounded result), FP32 for
+// FP16/BF16 tables.  The new momentum is rounded to FP32 (its stored type)
+// before it enters the denominator.
+template <typename ACC> struct Adagrad;
+template <> struct Adagrad<double> {
+    using G = double;   // type the row gradient enters the update in
+    static __device__ __forceinline__ G grad(double a) { return a; }
+    static __device__ __forceinline__ float mom(float m_old, double ss, int D) {
+        return (float)((double)m_old + ss / (double)D);
+    }
+    static __device__ __forceinline__ double den(float m_new, float eps) {
+        return sqrt((double)m_new) + (double)eps;
+    }
+    static __device__ __forceinline__ float step(float w, double g, float lr, double den) {
+        return (float)((double)w - (double)lr * g / den);
+    }
+};
+template <> struct Adagrad<float> {
+    using G = float;
+    static __device__ __forceinline__ G grad(float a) { return a; }
+    static __device__ __forceinline__ float mom(float m_old, float ss, int D) {
+        return __fadd_rn(m_old, __fdiv_rn(ss, (float)D));
+    }
+    static __device__ __forceinline__ float den(float m_new, float eps) {
+        return __fadd_rn(__fsqrt_rn(m_new), eps);
+    }
+    static __device__ __forceinline__ float step(float w, float g, float lr, float den) {
+        return __fsub_rn(w, __fdiv_rn(__fmul_rn(lr, g), den));
+    }
+};
+
+// Exact rowwise Adagrad on row `row` from the reduced gradient in acc.  Only
+// lanes of sub-group 0 hold meaningful values; every lane takes part in the
+// shuffles.
 template <typename WT, typename ACC, int LPR, int NV>
 __device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const BwdParams &p,
                                               int64_t row, int lane, int sub, int li) {
-    float gf[NV][4];
+    using A = Adagrad<ACC>;
     ACC ss = ACC(0);
 #pragma unroll
     for (int q = 0; q < NV; ++q)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            gf[q][x] = (float)acc[q][x];
-            ss += (ACC)gf[q][x] * (ACC)gf[q][x];
-        }
+        for (int x = 0; x < 4; ++x) ss += acc[q][x] * acc[q][x];
 #pragma unroll
     for (int sh = 1; sh < LPR; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
     if (sub != 0) return;
-    const float m_old = p.mom[row];
-    const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
-    const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+    const float m_new = A::mom(p.mom[row], ss, p.D);
+    const auto den = A::den(m_new, p.eps);
     WT *wr = reinterpret_cast<WT *>(p.W) + row * p.D + li * 4;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
         float w[4];
         ld4(wr + q * LPR * 4, w);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) w[x] = __fsub_rn(w[x], __fdiv_rn(__fmul_rn(p.lr, gf[q][x]), den));
+        for (int x = 0; x < 4; ++x) w[x] = A::step(w[x], acc[q][x], p.lr, den);
         st4(wr + q * LPR * 4, w);
     }
     if (lane == 0) p.mom[row] = m_new;
@@ -363,27 +392,23 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
             }
         }
         // exact rowwise Adagrad: m += mean_d g^2; w -= lr * g / (sqrt(m) + eps)
-        float gf[NV][4];
+        using A = Adagrad<ACC>;
         ACC ss = ACC(0);
 #pragma unroll
         for (int q = 0; q < NV; ++q)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                gf[q][x] = (float)acc[q][x];
-                ss += (ACC)gf[q][x] * (ACC)gf[q][x];
-            }
+            for (int x = 0; x < 4; ++x) ss += acc[q][x] * acc[q][x];
 #pragma unroll
         for (int o = 1; o < GL; o <<= 1) ss += __shfl_xor_sync(FULL, ss, o);
         if (mine) {
-            const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
-            const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+            const float m_new = A::mom(m_old, ss, p.D);
+            const auto den = A::den(m_new, p.eps);
 #pragma unroll
             for (int q = 0; q < NV; ++q) {
                 float w[4];
                 unpack<WT>(wraw[q], w);
 #pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    w[x] = __fsub_rn(w[x], __fdiv_rn(__fmul_rn(p.lr, gf[q][x]), den));
+                for (int x = 0; x < 4; ++x) w[x] = A::step(w[x], acc[q][x], p.lr, den);
                 st4(wr + (gl + q * GL) * 4, w);
             }
             if (gl == 0) p.mom[key] = m_new;
@@ -864,22 +889,23 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
                     wready = true;
                 }
                 const int slot = (int)(tag & 31u);
-                float gf[NV][4];
+                using A = Adagrad<ACC>;
+                ACC g[NV][4];
                 ACC ss = ACC(0);
 #pragma unroll
                 for (int q = 0; q < NV; ++q)
 #pragma unroll
                     for (int x2 = 0; x2 < 4; ++x2) {
-                        gf[q][x2] = (float)acc[q][x2];
-                        ss += (ACC)gf[q][x2] * (ACC)gf[q][x2];
+                        g[q][x2] = acc[q][x2];
+                        ss += g[q][x2] * g[q][x2];
                         acc[q][x2] = ACC(0);
                     }
 #pragma unroll
                 for (int sh = 1; sh < 32; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
                 const float m_old = __shfl_sync(FULL, cur.mom, slot);
                 const uint32_t key = __shfl_sync(FULL, cur.key, slot);
-                const float m_new = (float)((ACC)m_old + ss / (ACC)p.D);
-                const float den = __fadd_rn(__fsqrt_rn(m_new), p.eps);
+                const float m_new = A::mom(m_old, ss, p.D);
+                const auto den = A::den(m_new, p.eps);
                 const WT *wsrc = reinterpret_cast<const WT *>(wbuf + cw * SS_WBUF + slot * wrow) + lane * 4;
                 WT *wdst = reinterpret_cast<WT *>(p.W) + (int64_t)key * p.D + lane * 4;
 #pragma unroll
@@ -887,8 +913,7 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
                     float w[4];
                     ld4(wsrc + q * 128, w);
 #pragma unroll
-                    for (int x2 = 0; x2 < 4; ++x2)
-                        w[x2] = __fsub_rn(w[x2], __fdiv_rn(__fmul_rn(p.lr, gf[q][x2]), den));
+                    for (int x2 = 0; x2 < 4; ++x2) w[x2] = A::step(w[x2], g[q][x2], p.lr, den);
                     st4(wdst + q * 128, w);
                 }
                 if (lane == 0) p.mom[key] = m_new;
@@ -1081,6 +1106,28 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     default: return TBE_ERR_UNSUPPORTED_DTYPE;
     }
     return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the bulk-copy wait's time limit: one warp waits on an
+// mbarrier phase that nothing will complete (no copy is issued), gives up
+// after WAIT_LIMIT_NS and sets TBE_FLAG_COPY_TIMEOUT, as the gradient-row
+// rings do when a copy does not land.
+
+__global__ void __launch_bounds__(32) mbar_selftest_kernel(int32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) bar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    if (!mbar_wait_bounded(b, 0) && threadIdx.x == 0) atomicOr(status + 1, TBE_FLAG_COPY_TIMEOUT);
+}
+
+tbe_status launch_copy_wait_selftest(Launch &L, int32_t *status) {
+    L.before("tbe_selftest_copy_wait");
+    mbar_selftest_kernel<<<1, 32, 0, L.stream>>>(status);
+    L.after();
+    return TBE_OK;
 }
 
 }  // namespace tbe

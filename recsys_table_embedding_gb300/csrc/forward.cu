@@ -34,6 +34,7 @@ struct FwdParams {
     uint32_t *vals;
     int32_t *bag_of;
     int32_t *status;
+    int32_t *counters;   // nullable: C_MALFORMED / C_DECREASING
     int64_t B;
     int64_t NB;
     int64_t N;
@@ -91,6 +92,29 @@ template <int VEC, typename ACC> __device__ __forceinline__ void store_out(float
     }
 }
 
+// Well-formed bag: 0 <= start <= end <= N.  A malformed bag is made empty,
+// flagged in the status word and recorded in the counters (if any).
+__device__ __forceinline__ void check_bag(const FwdParams &p, int lane, int32_t &start, int32_t &end) {
+    if (start <= end && start >= 0 && (int64_t)end <= p.N) return;
+    if (lane == 0) {
+        atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
+        if (p.counters != nullptr) {
+            p.counters[C_MALFORMED] = 1;
+            if (end < start) p.counters[C_DECREASING] = 1;
+        }
+    }
+    start = end = 0;
+}
+
+// offsets[0] != 0 or offsets[T*B] != N leaves lookups outside every bag
+__device__ __forceinline__ void check_span(const FwdParams &p) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    if (__ldg(p.offsets) != 0 || (int64_t)__ldg(p.offsets + p.NB) != p.N) {
+        atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
+        if (p.counters != nullptr) p.counters[C_MALFORMED] = 1;
+    }
+}
+
 __device__ __forceinline__ int warp_sum_i(int v) {
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(FULL, v, s);
@@ -116,15 +140,13 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
     const int tstep = (int)(nwarps / p.B);
     const int64_t bstep = nwarps - (int64_t)tstep * p.B;
     int oob = 0;
+    check_span(p);
     for (; bag < p.NB; bag += nwarps) {
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
         int32_t start = __ldg(p.offsets + bag);
         int32_t end = __ldg(p.offsets + bag + 1);
-        if (end < start || start < 0 || (int64_t)end > p.N) {
-            if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
-            start = end = 0;   // malformed bag: empty
-        }
+        check_bag(p, lane, start, end);
         const bool wt = WEIGHTED && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         const WT *Wt = reinterpret_cast<const WT *>(p.W) + row0 * p.D + li * VEC;
         ACC acc[NV][VEC];
@@ -213,6 +235,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
 __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    check_span(p);
     for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < p.NB;
          bag += nwarps) {
         const int t = (int)(bag / p.B);
@@ -221,16 +244,46 @@ __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
         int32_t start = __ldg(p.offsets + bag);
         int32_t end = __ldg(p.offsets + bag + 1);
-        if (end < start || start < 0 || (int64_t)end > p.N) {
-            if (lane == 0) atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
-            start = end = 0;   // malformed bag: empty
-        }
+        check_bag(p, lane, start, end);
         for (int32_t i = start + lane; i < end; i += 32) {
             const int32_t idx = __ldg(p.indices + i);
             const bool valid = idx >= 0 && (int64_t)idx < E;
             p.keys[i] = valid ? (uint32_t)(row0 + idx) : p.sentinel;
             p.vals[i] = p.payload_pos ? (uint32_t)i : (uint32_t)b;
             if (p.bag_of != nullptr) p.bag_of[i] = (int32_t)bag;
+        }
+    }
+}
+
+// Runs after the forward or linearize kernel and does nothing unless that
+// kernel found the offsets malformed.  Then each lookup position p finds the
+// bag that would own it -- the last bag g with offsets[g] <= p, a binary
+// search that is exact while the offsets never decrease -- and, unless that
+// bag is well formed and holds p, gets the sentinel key (so the sort puts it
+// last and no run starts at it), payload 0 and bag -1.  When some bag ends
+// before it starts, two well-formed bags can hold one lookup, and every
+// lookup gets the sentinel: such a batch has no backward update.
+__global__ void __launch_bounds__(256) tbe_offsets_fixup_kernel(const FwdParams p) {
+    if (__ldg(p.counters + C_MALFORMED) == 0) return;
+    const bool decreasing = __ldg(p.counters + C_DECREASING) != 0;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.N; i += stride) {
+        bool covered = false;
+        if (!decreasing) {
+            // largest g in [0, NB] with offsets[g] <= i (none if offsets[0] > i)
+            int64_t lo = 0, hi = p.NB + 1;   // answer in [lo - 1, hi)
+            while (lo < hi) {
+                const int64_t mid = (lo + hi) >> 1;
+                if ((int64_t)__ldg(p.offsets + mid) <= i) lo = mid + 1; else hi = mid;
+            }
+            const int64_t g = lo - 1;
+            covered = g >= 0 && g < p.NB && __ldg(p.offsets + g) >= 0 &&
+                      (int64_t)__ldg(p.offsets + g + 1) <= p.N;
+        }
+        if (!covered) {
+            p.keys[i] = p.sentinel;
+            p.vals[i] = 0u;
+            if (p.bag_of != nullptr) p.bag_of[i] = -1;
         }
     }
 }
@@ -316,7 +369,8 @@ static bool fwd_dispatch(Launch &L, const FwdParams &p, int row_bytes) {
 }
 
 static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *out, uint32_t *keys,
-                             uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status) {
+                             uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status,
+                             int32_t *counters) {
     FwdParams p;
     p.W = tab->weights;
     p.table_offset = tab->table_offset;
@@ -329,6 +383,7 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
     p.vals = vals;
     p.bag_of = bag_of;
     p.status = status;
+    p.counters = counters;
     p.B = bt->B;
     p.NB = (int64_t)tab->T * bt->B;
     p.N = bt->N;
@@ -341,8 +396,8 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
 
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
                           uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
-                          int32_t *status) {
-    FwdParams p = make_params(tab, bt, out, keys, vals, bag_of, sentinel, status);
+                          int32_t *status, int32_t *counters) {
+    FwdParams p = make_params(tab, bt, out, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
     bool ok = false;
     if (!row_plan(tab->D, tab->dtype == TBE_F32 ? 4 : 2).ok) return TBE_ERR_UNSUPPORTED_DIM;
@@ -356,12 +411,27 @@ tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
 }
 
 tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt, uint32_t *keys,
-                            uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status) {
-    FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, status);
+                            uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status,
+                            int32_t *counters) {
+    FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
     const int grid = grid_for(tbe_linearize_kernel, 256, p.NB, L.num_sms);
     L.before("tbe_linearize");
     tbe_linearize_kernel<<<grid, 256, 0, L.stream>>>(p);
+    L.after();
+    return TBE_OK;
+}
+
+tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt, uint32_t *keys,
+                                uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+                                const int32_t *counters) {
+    FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, nullptr,
+                              const_cast<int32_t *>(counters));
+    if (p.N == 0) return TBE_OK;
+    int64_t grid = (p.N + 255) / 256;
+    if (grid > (int64_t)L.num_sms * 4) grid = (int64_t)L.num_sms * 4;
+    L.before("tbe_offsets_fixup");
+    tbe_offsets_fixup_kernel<<<(unsigned)grid, 256, 0, L.stream>>>(p);
     L.after();
     return TBE_OK;
 }

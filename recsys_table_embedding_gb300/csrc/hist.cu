@@ -137,6 +137,7 @@ struct HistFwdParams {
     float *out;
     uint16_t *hist;       // nullable
     int32_t *status;
+    int32_t *counters;    // nullable: C_MALFORMED / C_DECREASING
     int64_t B;
     int64_t N;
     int T;
@@ -155,10 +156,9 @@ struct HistFwdSmem {
     alignas(1024) unsigned char A[HT_BAGS * 128];   // counts as FP16, [128 bags][64 rows]
     uint32_t cnt[HT_BAGS * CNT_STRIDE];             // two 16-bit counts per word
     alignas(1024) unsigned char Bm[128 * 128];      // W_t^T, [D][64 rows]
-    int32_t offs[HT_BAGS + 1];
+    int32_t bs[HT_BAGS], be[HT_BAGS];               // lookup range of each bag (empty if malformed)
     uint64_t mbar;
     uint32_t tmem_base;
-    int32_t bad;
 };
 
 __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdParams p) {
@@ -190,6 +190,12 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
     bool alive = true;
     int cur_t = -1;
     int oob = 0;
+    // offsets[0] != 0 or offsets[T*B] != N leaves lookups outside every bag
+    if (blockIdx.x == 0 && tid == 0 &&
+        (__ldg(p.offsets) != 0 || (int64_t)__ldg(p.offsets + p.T * p.B) != p.N)) {
+        atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
+        if (p.counters != nullptr) p.counters[C_MALFORMED] = 1;
+    }
 
     for (int64_t tile = tile0; tile < tile1 && alive; ++tile) {
         const int t = (int)(tile / p.tiles_per_table);
@@ -210,23 +216,25 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
             cur_t = t;
         }
         for (int i = tid; i < HT_BAGS * CNT_STRIDE; i += HF_THREADS) S.cnt[i] = 0;
-        if (tid == 0) S.bad = 0;
-        if (tid <= HT_BAGS) {
-            const int j = tid <= nb ? tid : nb;
-            int32_t o = __ldg(p.offsets + g0 + j);
-            S.offs[tid] = o;
+        if (tid < HT_BAGS) {
+            // a well-formed bag has 0 <= start <= end <= N; any other is empty
+            int32_t s0 = 0, s1 = 0;
+            if (tid < nb) {
+                s0 = __ldg(p.offsets + g0 + tid);
+                s1 = __ldg(p.offsets + g0 + tid + 1);
+                if (!(s0 <= s1 && s0 >= 0 && (int64_t)s1 <= p.N)) {
+                    atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
+                    if (p.counters != nullptr) {
+                        p.counters[C_MALFORMED] = 1;
+                        if (s1 < s0) p.counters[C_DECREASING] = 1;
+                    }
+                    s0 = s1 = 0;
+                }
+            }
+            S.bs[tid] = s0;
+            S.be[tid] = s1;
         }
         __syncthreads();
-        if (tid < nb) {
-            const int32_t s0 = S.offs[tid], s1 = S.offs[tid + 1];
-            if (s1 < s0 || s0 < 0 || (int64_t)s1 > p.N) S.bad = 1;
-        }
-        __syncthreads();
-        if (S.bad) {
-            if (tid == 0) atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
-            if (tid <= HT_BAGS) S.offs[tid] = 0;   // treat the tile's bags as empty
-            __syncthreads();
-        }
         // count the tile's lookups: a warp takes CB bags at a time and its
         // lanes read CU*32 consecutive lookups of each (CB*CU loads in flight
         // per lane); every lookup adds one to its bag's 16-bit row counter
@@ -239,8 +247,8 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
 #pragma unroll
                 for (int j = 0; j < CB; ++j) {
                     const int r = r0 + j;
-                    bs[j] = r < nb ? S.offs[r] : 0;
-                    be[j] = r < nb ? S.offs[r + 1] : 0;
+                    bs[j] = r < nb ? S.bs[r] : 0;
+                    be[j] = r < nb ? S.be[r] : 0;
                     maxlen = max(maxlen, be[j] - bs[j]);
                 }
                 for (int32_t k = 0; k < maxlen; k += 32 * CU) {
@@ -272,7 +280,7 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
         {
             const int r = tid & (HT_BAGS - 1), h = tid >> 7;
             // a 16-bit count could wrap only in a bag of more than 65535 lookups
-            int over = h == 0 && r < nb && S.offs[r + 1] - S.offs[r] > 65535;
+            int over = h == 0 && r < nb && S.be[r] - S.bs[r] > 65535;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c = h * 4 + cc;
@@ -380,6 +388,7 @@ struct HistBwdParams {
     float *cnt;           // [T][S][64] slice counts
     int32_t *arrive;      // [T]
     int32_t *status;
+    const int32_t *counters;   // nullable: no update when C_DECREASING is set
     int64_t B;
     int T;
     int D;
@@ -413,6 +422,8 @@ __global__ void __launch_bounds__(HB_THREADS) tbe_hist_bwd_kernel(const HistBwdP
     if (be > p.B) be = p.B;
     const int nsteps = be > bb ? (int)((be - bb + HB_KBAGS - 1) / HB_KBAGS) : 0;
     const int64_t TD = (int64_t)p.T * p.D;
+    // offsets that decrease leave lookups in two bags: no backward update
+    if (p.counters != nullptr && __ldg(p.counters + C_DECREASING) != 0) return;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, 64);
@@ -632,9 +643,11 @@ static size_t fwd_smem() { return sizeof(HistFwdSmem) + 1024; }
 static size_t bwd_smem() { return sizeof(HistBwdSmem) + 1024; }
 
 static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
-                                  float *out, uint16_t *hist, int32_t *status, int do_mma) {
+                                  float *out, uint16_t *hist, int32_t *status, int32_t *counters,
+                                  int do_mma) {
     if (bt->B == 0) return TBE_OK;
     HistFwdParams p;
+    p.counters = counters;
     p.W = reinterpret_cast<const __half *>(tab->weights);
     p.table_offset = tab->table_offset;
     p.indices = bt->indices;
@@ -669,20 +682,22 @@ static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_ba
 }
 
 tbe_status launch_hist_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
-                               uint16_t *hist, int32_t *status) {
-    return hist_fwd_launch(L, tab, bt, out, hist, status, 1);
+                               uint16_t *hist, int32_t *status, int32_t *counters) {
+    return hist_fwd_launch(L, tab, bt, out, hist, status, counters, 1);
 }
 
 tbe_status launch_hist_count(Launch &L, const tbe_tables *tab, const tbe_batch *bt, uint16_t *hist,
-                             int32_t *status) {
-    return hist_fwd_launch(L, tab, bt, nullptr, hist, status, 0);
+                             int32_t *status, int32_t *counters) {
+    return hist_fwd_launch(L, tab, bt, nullptr, hist, status, counters, 0);
 }
 
 tbe_status launch_hist_backward(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
                                 const uint16_t *hist, float *momentum, const float *grad_out,
-                                float lr, float eps, void *ws, int32_t *status) {
+                                float lr, float eps, void *ws, int32_t *status,
+                                const int32_t *counters) {
     if (bt->B == 0) return TBE_OK;
     HistBwdParams p;
+    p.counters = counters;
     p.W = reinterpret_cast<__half *>(tab->weights);
     p.mom = momentum;
     p.G = grad_out;

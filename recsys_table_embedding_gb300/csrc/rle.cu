@@ -68,11 +68,13 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const uint32_t *
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
         if (pos < N) {
+            // keys >= sentinel (out-of-range lookups and lookups outside every
+            // well-formed bag; they sort last) start no run
             const uint32_t cur = __ldg(k + pos);
             const bool first = pos == 0 || cur != prev;
-            if (first && cur != sentinel) ++heads;
-            if (cur == sentinel && first) counters[C_N_VALID] = (int32_t)pos;
-            if (pos == N - 1 && cur != sentinel) counters[C_N_VALID] = (int32_t)N;
+            if (first && cur < sentinel) ++heads;
+            if (cur >= sentinel && (pos == 0 || prev < sentinel)) counters[C_N_VALID] = (int32_t)pos;
+            if (pos == N - 1 && cur < sentinel) counters[C_N_VALID] = (int32_t)N;
             prev = cur;
         }
     }
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
         kk[i] = pos < N ? __ldg(k + pos) : sentinel;
-        if (pos < N && (pos == 0 || kk[i] != prev) && kk[i] != sentinel) headmask |= 1u << i;
+        if (pos < N && (pos == 0 || kk[i] != prev) && kk[i] < sentinel) headmask |= 1u << i;
         prev = kk[i];
     }
     int total;
@@ -253,10 +255,14 @@ __global__ void zero_counters_kernel(int32_t *counters) {
 
 __global__ void zero_first_kernel(int32_t *p) { p[0] = 0; }
 
-tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
-    L.before("tbe_rle_zero");
-    zero_counters_kernel<<<1, 32, 0, L.stream>>>(a.counters);
+void launch_zero_counters(Launch &L, int32_t *counters) {
+    L.before("tbe_zero_counters");
+    zero_counters_kernel<<<1, 32, 0, L.stream>>>(counters);
     L.after();
+}
+
+// The counters were zeroed before the forward or linearize kernel.
+tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     if (a.N == 0) {
         // seg_off[0] = 0 for an empty batch
         L.before("tbe_rle_zero");

@@ -333,4 +333,47 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
     return TBE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the look-back's time limit.  Two tiles of zero keys; the tile
+// ticket starts at 1, so the one CTA launched takes tile 1 and looks back at
+// tile 0, which no CTA will ever publish.  After WAIT_LIMIT_NS the CTA sets
+// TBE_FLAG_SORT_TIMEOUT and finishes its tile (every write stays inside the
+// two-tile buffers; the output is invalid, as the flag says).  No copy is in
+// flight during the wait.
+
+constexpr int64_t SELFTEST_N = 2 * SORT_TILE;
+
+size_t sort_selftest_bytes() {
+    return (size_t)4 * SELFTEST_N * 4 + RADIX * 4 + 2 * RADIX * 4 + 256;
+}
+
+__global__ void sort_selftest_init_kernel(uint32_t *words, int64_t n, uint32_t *ticket) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        words[i] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 1;
+}
+
+tbe_status launch_sort_selftest(Launch &L, void *ws, int32_t *status) {
+    uint32_t *w = (uint32_t *)ws;
+    uint32_t *keys_in = w, *vals_in = w + SELFTEST_N, *keys_out = w + 2 * SELFTEST_N,
+             *vals_out = w + 3 * SELFTEST_N;
+    uint32_t *bucket = w + 4 * SELFTEST_N;
+    uint32_t *look = bucket + RADIX;
+    uint32_t *ticket = look + 2 * RADIX;
+    const int64_t words = 4 * SELFTEST_N + 3 * RADIX;
+    L.before("tbe_selftest_init");
+    sort_selftest_init_kernel<<<8, 256, 0, L.stream>>>(w, words, ticket);
+    L.after();
+    const size_t smem = sizeof(PassSmem);
+    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    L.before("tbe_sort_onesweep");
+    radix_onesweep_kernel<<<1, SORT_THREADS, smem, L.stream>>>(keys_in, vals_in, keys_out, vals_out,
+                                                                SELFTEST_N, 0, RADIX - 1, bucket,
+                                                                look, ticket, status + 1);
+    L.after();
+    return TBE_OK;
+}
+
 }  // namespace tbe

@@ -198,12 +198,16 @@ static tbe_status finish(const Launch &L, tbe_status st) {
     return L.failed ? TBE_ERR_CUDA : TBE_OK;
 }
 
-// linearize (unless the forward already did) + sort + RLE/route, generic path
+// After the forward or linearize kernel wrote keys and payloads: the
+// malformed-offsets fixup, sort, RLE/route (generic path)
 static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
                                 tbe_meta *meta, const Problem &pr, void *ws, int32_t *status) {
+    tbe_status st = launch_offsets_fixup(L, tab, bt, meta->keys_a, meta->vals_a, meta->bag_of,
+                                         (uint32_t)pr.rows_total, meta->counters);
+    if (st != TBE_OK) return st;
     bool in_b = false;
-    tbe_status st = launch_sort(L, meta->keys_a, meta->vals_a, meta->keys_b, meta->vals_b, pr.N,
-                                pr.key_bits, ws, status, &in_b);
+    st = launch_sort(L, meta->keys_a, meta->vals_a, meta->keys_b, meta->vals_b, pr.N, pr.key_bits,
+                     ws, status, &in_b);
     if (st != TBE_OK) return st;
     meta->sorted_keys = in_b ? meta->keys_b : meta->keys_a;
     meta->sorted_vals = in_b ? meta->vals_b : meta->vals_a;
@@ -325,13 +329,15 @@ tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *
     }
     Launch L(stream, cfg);
     L.num_sms = sm_count();
+    if (meta != nullptr) launch_zero_counters(L, meta->counters);
     if (pr.path == 2) {
-        st = launch_hist_forward(L, tables, batch, out, meta ? meta->hist : nullptr, dev_status);
+        st = launch_hist_forward(L, tables, batch, out, meta ? meta->hist : nullptr, dev_status,
+                                 meta ? meta->counters : nullptr);
         return finish(L, st);
     }
     st = launch_forward(L, tables, batch, out, meta ? meta->keys_a : nullptr,
                         meta ? meta->vals_a : nullptr, meta ? meta->bag_of : nullptr,
-                        (uint32_t)pr.rows_total, dev_status);
+                        (uint32_t)pr.rows_total, dev_status, meta ? meta->counters : nullptr);
     if (st == TBE_OK && meta != nullptr)
         st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
     return finish(L, st);
@@ -348,9 +354,11 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
     if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
     Launch L(stream, cfg);
     L.num_sms = sm_count();
-    if (pr.path == 2) return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status));
+    launch_zero_counters(L, meta->counters);
+    if (pr.path == 2)
+        return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status, meta->counters));
     st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
-                          (uint32_t)pr.rows_total, dev_status);
+                          (uint32_t)pr.rows_total, dev_status, meta->counters);
     if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
     return finish(L, st);
 }
@@ -374,7 +382,7 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
     L.num_sms = sm_count();
     if (pr.path == 2)
         return finish(L, launch_hist_backward(L, tables, batch, meta->hist, momentum, grad_out, lr,
-                                              eps, workspace, dev_status));
+                                              eps, workspace, dev_status, meta->counters));
     BwdArgs a;
     a.tab = tables;
     a.bt = batch;
@@ -415,7 +423,23 @@ const char *tbe_status_string(tbe_status s) {
     return "unknown status";
 }
 
-int32_t tbe_version(void) { return 100; }
+int32_t tbe_version(void) { return 200; }
+
+size_t tbe_selftest_workspace_bytes(void) { return sort_selftest_bytes(); }
+
+tbe_status tbe_selftest_wait_limit(int32_t kind, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, cudaStream_t stream) {
+    if (dev_status == nullptr) return TBE_ERR_NULL_POINTER;
+    if (kind != TBE_SELFTEST_SORT_LOOKBACK && kind != TBE_SELFTEST_COPY_WAIT)
+        return TBE_ERR_INVALID_ARGUMENT;
+    Launch L(stream, nullptr);
+    L.num_sms = sm_count();
+    if (kind == TBE_SELFTEST_COPY_WAIT) return finish(L, launch_copy_wait_selftest(L, dev_status));
+    if (workspace == nullptr) return TBE_ERR_NULL_POINTER;
+    if (!aligned(workspace, 256)) return TBE_ERR_MISALIGNED;
+    if (workspace_bytes < sort_selftest_bytes()) return TBE_ERR_BUFFER_TOO_SMALL;
+    return finish(L, launch_sort_selftest(L, workspace, dev_status));
+}
 
 }  // extern "C"
 
@@ -475,16 +499,19 @@ extern "C" tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_
     size_t need = sort_workspace_bytes(pr.N, pr.key_bits);
     if (rle_workspace_bytes(pr.N) > need) need = rle_workspace_bytes(pr.N);
     if (need > STATIC_SCRATCH_BYTES) return TBE_ERR_SCRATCH_LIMIT;
-    void *scratch = nullptr;
-    if ((st = static_scratch(&scratch)) != TBE_OK) return st;
     Launch L(stream, cfg);
     L.num_sms = sm_count();
-    if (pr.path == 2) return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status));
+    launch_zero_counters(L, meta->counters);
+    // the histogram path's counting needs no scratch
+    if (pr.path == 2)
+        return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status, meta->counters));
+    void *scratch = nullptr;
+    if ((st = static_scratch(&scratch)) != TBE_OK) return st;
     // The sort zeroes its digit counts, tile tickets and look-back words, and
     // the RLE writes its tile counts before reading them, so the contents a
     // previous call left in the array are never read.
     st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
-                          (uint32_t)pr.rows_total, dev_status);
+                          (uint32_t)pr.rows_total, dev_status, meta->counters);
     if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, scratch, dev_status);
     return finish(L, st);
 }

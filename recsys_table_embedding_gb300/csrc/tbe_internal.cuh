@@ -12,8 +12,19 @@ namespace tbe {
 
 constexpr unsigned FULL = 0xffffffffu;
 
-// Indices into meta->counters (device int32).
-enum Counter { C_NUM_UNIQUE = 0, C_N_VALID = 1, C_NUM_LONG = 2, C_NUM_CHUNKS = 3, C_COUNT = 8 };
+// Indices into meta->counters (device int32).  C_MALFORMED is set when the
+// batch's offsets are malformed in any way (a bag not 0 <= start <= end <= N,
+// or offsets[0] != 0, or offsets[T*B] != N); C_DECREASING when some bag has
+// end < start.  Both are zeroed before the forward or linearize kernel runs.
+enum Counter {
+    C_NUM_UNIQUE = 0,
+    C_N_VALID = 1,
+    C_NUM_LONG = 2,
+    C_NUM_CHUNKS = 3,
+    C_MALFORMED = 4,
+    C_DECREASING = 5,
+    C_COUNT = 8
+};
 
 // Weight element traits: the 16-byte vector of a row, and the accumulator
 // precision (FBTriton TBE redesign, decision checklist item 1: FP32 for
@@ -127,12 +138,22 @@ struct RowPlan {
 RowPlan row_plan(int D, int bytes_per_elem);
 
 // --- forward.cu
+// `counters` (nullable) receives C_MALFORMED / C_DECREASING.
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
                           uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
-                          int32_t *status);
+                          int32_t *status, int32_t *counters);
 tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
                             uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
-                            int32_t *status);
+                            int32_t *status, int32_t *counters);
+// After the forward or linearize kernel: when counters[C_MALFORMED] is set,
+// every lookup outside a well-formed bag gets the sentinel key (all lookups
+// when counters[C_DECREASING] is set), so that only lookups of well-formed
+// bags reach the backward.  Does nothing on well-formed batches.
+tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
+                                uint32_t *keys, uint32_t *vals, int32_t *bag_of,
+                                uint32_t sentinel, const int32_t *counters);
+// zero meta->counters (all C_COUNT words)
+void launch_zero_counters(Launch &L, int32_t *counters);
 
 // --- sort.cu: stable LSD radix sort of (key, val) pairs over the low
 // `key_bits` bits; result lands in (keys_a, vals_a) when the number of
@@ -141,6 +162,10 @@ size_t sort_workspace_bytes(int64_t N, int key_bits);
 tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *keys_b,
                        uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
                        bool *in_b);
+
+// Self-test of the look-back's time limit (scratch of sort_selftest_bytes()).
+size_t sort_selftest_bytes();
+tbe_status launch_sort_selftest(Launch &L, void *ws, int32_t *status);
 
 // --- rle.cu: run-length encode sorted keys, route long runs into chunks.
 size_t rle_workspace_bytes(int64_t N);
@@ -194,16 +219,22 @@ struct BwdArgs {
 };
 size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype);
 tbe_status launch_backward(Launch &L, const BwdArgs &a);
+// Self-test of the bulk-copy wait's time limit.
+tbe_status launch_copy_wait_selftest(Launch &L, int32_t *status);
 
 // --- hist.cu: small-table histogram path on the tensor cores
 bool hist_shape_ok(const tbe_tables *tab, const tbe_batch *bt, int64_t max_rows);
 size_t hist_workspace_bytes(const tbe_tables *tab, const tbe_batch *bt);
+// `counters` (nullable; the meta's) receives C_MALFORMED / C_DECREASING in
+// the forward and count kernels; the backward applies no update when
+// counters[C_DECREASING] is set.
 tbe_status launch_hist_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
-                               uint16_t *hist, int32_t *status);
+                               uint16_t *hist, int32_t *status, int32_t *counters);
 tbe_status launch_hist_count(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
-                             uint16_t *hist, int32_t *status);
+                             uint16_t *hist, int32_t *status, int32_t *counters);
 tbe_status launch_hist_backward(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
                                 const uint16_t *hist, float *momentum, const float *grad_out,
-                                float lr, float eps, void *ws, int32_t *status);
+                                float lr, float eps, void *ws, int32_t *status,
+                                const int32_t *counters);
 
 }  // namespace tbe

@@ -26,15 +26,17 @@ F32, F16, BF16 = 0, 1, 2
 LONG_AUTO, LONG_TWO_KERNEL, LONG_FUSED = 0, 1, 2
 HIST_AUTO, HIST_OFF, HIST_FORCE = 0, 1, 2
 STATUS_WORDS = 4
-FLAG_BAD_OFFSETS, FLAG_FP16_OVERFLOW, FLAG_SORT_TIMEOUT, FLAG_HIST_COUNT, FLAG_MMA_TIMEOUT = (
-    0x1, 0x2, 0x4, 0x8, 0x10)
+(FLAG_BAD_OFFSETS, FLAG_FP16_OVERFLOW, FLAG_SORT_TIMEOUT, FLAG_HIST_COUNT, FLAG_MMA_TIMEOUT,
+ FLAG_COPY_TIMEOUT) = (0x1, 0x2, 0x4, 0x8, 0x10, 0x20)
 
 _TORCH_DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTED = ("tbe_config_default", "tbe_query_sizes", "tbe_meta_bind", "tbe_forward",
             "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_select_path",
             "tbe_status_string", "tbe_status_str", "tbe_version", "tbe_preprocess_static",
-            "tbe_workspace_bytes", "tbe_meta_bytes")
+            "tbe_workspace_bytes", "tbe_meta_bytes", "tbe_selftest_workspace_bytes",
+            "tbe_selftest_wait_limit")
+SELFTEST_SORT_LOOKBACK, SELFTEST_COPY_WAIT = 0, 1
 STATIC_SCRATCH_MAX_N = 1 << 22
 
 
@@ -107,6 +109,10 @@ def lib():
         L.tbe_status_str.argtypes = [i32]
         L.tbe_workspace_bytes.restype = ctypes.c_size_t
         L.tbe_meta_bytes.restype = ctypes.c_size_t
+        L.tbe_selftest_workspace_bytes.restype = ctypes.c_size_t
+        L.tbe_selftest_workspace_bytes.argtypes = []
+        L.tbe_selftest_wait_limit.restype = i32
+        L.tbe_selftest_wait_limit.argtypes = [i32, P, ctypes.c_size_t, P, P]
         _lib = L
     return _lib
 
@@ -231,6 +237,16 @@ def tbe_backward_rowwise_adagrad(tables: Tables, batch: Batch, momentum: torch.T
         ctypes.byref(tables.c), ctypes.byref(batch.c), momentum.data_ptr(), grad_out.data_ptr(),
         ctypes.byref(meta.c), float(lr), float(eps), workspace.data_ptr(), workspace.numel(),
         dev_status.data_ptr(), ctypes.byref(cfg) if cfg else None, _stream(stream)))
+
+
+def tbe_selftest_wait_limit(kind: int, dev_status: torch.Tensor, stream=None):
+    """Run one device wait that nothing ends (see include/tbe.h); the wait
+    gives up after one second and sets its flag in dev_status[1]."""
+    ws = torch.empty(int(lib().tbe_selftest_workspace_bytes()), dtype=torch.uint8,
+                     device=dev_status.device)
+    _check(lib().tbe_selftest_wait_limit(int(kind), ws.data_ptr(), ws.numel(), dev_status.data_ptr(),
+                                         _stream(stream)))
+    return ws
 
 
 class TBE:

@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Largest observed error of each compared quantity, relative to its
+    stated bar (filled by the parity helpers during the GPU tests)."""
+    try:
+        import parity
+    except Exception:
+        return
+    if parity.REPORT:
+        terminalreporter.write_sep("-", "parity: max observed error / stated bar")
+        for k in sorted(parity.REPORT):
+            terminalreporter.write_line(f"{k}: {parity.REPORT[k]:.4g}")

@@ -1,19 +1,31 @@
 """Shared helpers of the parity tests: run the CUDA path through the C ABI,
 run the oracle on the same seeded inputs, compare with the stated tolerances.
 
-Tolerances (the stated bars, read for the cases they leave open):
+The stated bars, asserted element by element:
   * batch inversion (sorted keys/payloads, unique keys, segment offsets,
     counts): bit-exact.
-  * forward output: |dev - ref| <= rtol * S where S = sum_p |w_p W[idx_p, d]|
-    is the oracle's sum of magnitudes (S = |ref| when nothing cancels);
-    rtol = 1e-4, or 1e-6 for FP32 tables.  Any summation order of the terms
-    stays inside n * 2^-24 * S for FP32 accumulation.
-  * momentum: |dev - ref| <= 1e-4 |ref| (all its terms are non-negative).
-  * FP32 weights: |dev - ref| <= 1e-6 * max(|ref|, |W_old|), the scale of the
-    operands of the final subtraction W_old - update.
-  * FP16/BF16 weights: |dev - ref| <= 1 ulp of the stored type at
-    max(|ref|, |W_old|).
+  * forward output: |dev - ref| <= 1e-4 |ref|, with a floor of
+    1e-6 max|ref| for elements that cancel to near zero.
+  * momentum: |dev - ref| <= 1e-4 |ref|.
+  * FP32 weights: |dev - ref| <= 1e-6 |ref| (+ the FP64 arithmetic bound
+    below, which is ~1e-18 and matters only for a weight that cancels to
+    almost exactly zero).
+  * FP16/BF16 weights: |dev - ref| <= 1 ulp of the stored type at |ref|,
+    plus the error bound E of the arithmetic the pages prescribe for these
+    tables (FP32 accumulation of the row gradient, decision checklist item 1;
+    FP32 optimizer arithmetic): where the update nearly cancels the old
+    weight, a correct FP32 kernel can land more than one ulp of the small
+    result away from the exact one.  E is derived from the oracle's row
+    gradient g, the sum A of its terms' magnitudes and the run length n
+    (see ``w_arith_bound``); the tests report how many elements needed it.
   * rows no lookup touches: weights and momentum bit-identical to the input.
+
+Second reading, also asserted (kept from the scale-aware bars): forward
+within rtol * S, S = sum_p |w_p W[idx_p, d]| (rtol 1e-4, 1e-6 for FP32
+tables), and weights within 1 ulp (rel 1e-6) of max(|ref|, |W_old|).
+
+``REPORT`` collects the largest observed error of each quantity relative to
+its stated bar; the tests print it.
 """
 from __future__ import annotations
 
@@ -23,8 +35,19 @@ import torch
 import oracle
 
 OUT_RTOL = {"f32": 1e-6, "f16": 1e-4, "bf16": 1e-4}
+OUT_STATED_RTOL = 1e-4
+OUT_FLOOR = 1e-6
 MOM_RTOL = 1e-4
 W32_RTOL = 1e-6
+U32 = 2.0 ** -24
+U64 = 2.0 ** -53
+
+REPORT: dict = {}
+
+
+def _record(name, ratio):
+    if ratio.size:
+        REPORT[name] = max(REPORT.get(name, 0.0), float(np.max(ratio)))
 
 
 def wbits_np(W: torch.Tensor, dtype: str) -> np.ndarray:
@@ -51,20 +74,32 @@ def ulp(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def assert_out_close(dev: np.ndarray, ref: np.ndarray, absum: np.ndarray, dtype: str):
-    rtol = OUT_RTOL[dtype]
-    err = np.abs(dev.astype(np.float64) - ref.astype(np.float64))
-    bound = rtol * absum + 1e-30
+    dev = dev.astype(np.float64)
+    ref = ref.astype(np.float64)
+    err = np.abs(dev - ref)
+    # stated bar: rel 1e-4, floor 1e-6 max|ref| for near-zero elements
+    amax = float(np.max(np.abs(ref))) if ref.size else 0.0
+    stated = np.maximum(OUT_STATED_RTOL * np.abs(ref), OUT_FLOOR * amax)
+    bad = err > stated
+    _record("out/stated_bar", err / np.maximum(stated, 1e-300))
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"forward out: {int(bad.sum())} elements off the stated bar, first at "
+                             f"{i}: dev={dev[i]!r} ref={ref[i]!r} bar={stated[i]!r}")
+    # scale-aware bar: any summation order is within n 2^-24 S
+    bound = OUT_RTOL[dtype] * absum + 1e-30
     bad = err > bound
     if bad.any():
-        i = np.argwhere(bad)[0]
-        raise AssertionError(f"forward out: {int(bad.sum())} elements off, first at {tuple(i)}: "
-                             f"dev={dev[tuple(i)]!r} ref={ref[tuple(i)]!r} bound={bound[tuple(i)]!r}")
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"forward out: {int(bad.sum())} elements off, first at {i}: "
+                             f"dev={dev[i]!r} ref={ref[i]!r} bound={bound[i]!r}")
 
 
 def assert_momentum_close(dev: np.ndarray, ref: np.ndarray, m0: np.ndarray, touched: np.ndarray):
     np.testing.assert_array_equal(dev[~touched], m0[~touched], err_msg="untouched momentum changed")
     err = np.abs(dev[touched].astype(np.float64) - ref[touched].astype(np.float64))
     bound = MOM_RTOL * np.abs(ref[touched].astype(np.float64))
+    _record("momentum/stated_bar", err / np.maximum(bound, 1e-300))
     bad = err > bound
     if bad.any():
         i = np.argwhere(bad)[0][0]
@@ -72,16 +107,73 @@ def assert_momentum_close(dev: np.ndarray, ref: np.ndarray, m0: np.ndarray, touc
                              f"ref={ref[touched][i]!r}")
 
 
+def w_arith_bound(dtype: str, g: np.ndarray, A: np.ndarray, n: np.ndarray, m_old: np.ndarray,
+                  w_old: np.ndarray, lr: float, eps: float, path: int = 1) -> np.ndarray:
+    """Bound on |w - w_exact| before the final rounding to the stored type,
+    for the arithmetic the kernels are specified to use, per element [k, D].
+
+    g, A: the exact row gradient and the sum of its terms' magnitudes [k, D];
+    n: lookups of each row [k]; m_old: momentum before the step [k]; w_old:
+    weights before the step [k, D].  Unit roundoff u = 2^-53 for FP32 tables
+    (FP64 accumulation and optimizer), 2^-24 otherwise (FP32).  First-order
+    error propagation, doubled:
+      |g~ - g| <= d = gamma_n A,  gamma_n = (n + n/256 + 4) u  (terms, chunk
+                   partials and lane combines)
+      histogram path: + 2^-21 A + n 2^-24 (FP16 hi/lo split of the gradient)
+      m = m_old + sum_d g^2 / D, relative error e_m from d and D-term sums
+      den = sqrt(m) + eps, relative error e_den = (e_m/2 + u) sqrt(m)/den + u
+      upd = lr g / den:  |upd~ - upd| <= |upd| (2u + e_den) + lr d / den
+      w = w_old - upd:   + u (|w_old| + |upd|)
+    """
+    u = U64 if dtype == "f32" else U32
+    g = np.asarray(g, np.float64)
+    A = np.asarray(A, np.float64)
+    n = np.asarray(n, np.float64)[:, None]
+    D = g.shape[1]
+    delta = (n + n / 256.0 + 4.0) * u * 1.01 * A
+    if path == 2:
+        delta = delta + 2.0 ** -21 * A + n * 2.0 ** -24
+    ss = np.sum(g * g, axis=1)
+    m = np.asarray(m_old, np.float64) + ss / D
+    gam_d = (D + 4) * u
+    num = u * m + u * ss / D + (gam_d * ss + np.sum(2 * np.abs(g) * delta + delta * delta, axis=1)) / D
+    e_m = np.where(m > 0, num / np.where(m > 0, m, 1.0), 0.0)
+    sq = np.sqrt(m)
+    den = sq + eps
+    e_den = (e_m / 2 + u) * sq / den + u
+    upd = lr * np.abs(g) / den[:, None]
+    E = u * (np.abs(w_old) + upd) + upd * (2 * u + e_den[:, None]) + lr * delta / den[:, None]
+    return 2.0 * E
+
+
 def assert_weights_close(dev_bits: np.ndarray, ref_bits: np.ndarray, old_bits: np.ndarray,
-                         touched: np.ndarray, dtype: str):
+                         touched: np.ndarray, dtype: str, arith: np.ndarray = None):
+    """arith: w_arith_bound for the touched rows (in row order), or None to
+    assert only the scale-aware second reading."""
     np.testing.assert_array_equal(dev_bits[~touched], old_bits[~touched],
                                   err_msg="untouched weight rows changed")
     d = wvals_np(dev_bits[touched], dtype)
     r = wvals_np(ref_bits[touched], dtype)
     o = wvals_np(old_bits[touched], dtype)
+    err = np.abs(d - r)
+    if arith is not None:
+        if dtype == "f32":
+            stated = W32_RTOL * np.abs(r)
+            _record("W_f32/stated_bar", err / np.maximum(stated, 1e-300))
+            bar = stated + arith
+        else:
+            stated = ulp(r, dtype)
+            _record(f"W_{dtype}/ulps_of_ref", err / stated)
+            REPORT[f"W_{dtype}/elements_beyond_1ulp"] = (
+                REPORT.get(f"W_{dtype}/elements_beyond_1ulp", 0) + int(np.sum(err > stated)))
+            bar = ulp(np.abs(r) + arith, dtype) + arith
+        bad = err > bar
+        if bad.any():
+            i = tuple(np.argwhere(bad)[0])
+            raise AssertionError(f"weights: {int(bad.sum())} elements off the stated bar, first {i}: "
+                                 f"dev={d[i]!r} ref={r[i]!r} old={o[i]!r} bar={bar[i]!r}")
     scale = np.maximum(np.abs(r), np.abs(o))
     bound = W32_RTOL * scale if dtype == "f32" else ulp(scale, dtype)
-    err = np.abs(d - r)
     bad = err > bound
     if bad.any():
         i = tuple(np.argwhere(bad)[0])
@@ -107,13 +199,17 @@ def device_batch(wl, device="cuda"):
 
 
 def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
-             preprocess_in_forward=True, device="cuda"):
-    """One forward + backward through the C ABI.  Returns a dict of host arrays."""
+             preprocess_in_forward=True, device="cuda", meta_fill=None):
+    """One forward + backward through the C ABI.  Returns a dict of host arrays.
+    meta_fill (a byte value) fills the metadata buffer before the first call,
+    in place of whatever a fresh device allocation holds."""
     from recsys_table_embedding_gb300 import TBE, Tables, meta_view
     W = W0.to(device).contiguous()
     tables = Tables(W, wl.table_offset)
     batch = device_batch(wl, device)
     tbe = TBE(tables, batch, cfg, preprocess_in_forward=preprocess_in_forward)
+    if meta_fill is not None:
+        tbe.meta_buf.fill_(meta_fill)
     out = tbe.forward(batch)
     mom = torch.from_numpy(m0).to(device)
     Gd = torch.from_numpy(G).to(device)
@@ -133,8 +229,11 @@ def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
     return res
 
 
-def bag_of_position(wl) -> np.ndarray:
-    return np.repeat(np.arange(wl.NB, dtype=np.int64), np.diff(wl.offsets.astype(np.int64)))
+def bag_of_position(wl, pos: np.ndarray) -> np.ndarray:
+    """Bag id t*B+b of the given lookup positions, each of which lies in a
+    well-formed bag (every position the inversion keeps does, and offsets
+    then never decrease, so a binary search finds the bag)."""
+    return np.searchsorted(wl.offsets.astype(np.int64), pos, side="right") - 1
 
 
 def check_inversion(wl, res, pre):
@@ -147,7 +246,7 @@ def check_inversion(wl, res, pre):
     if res["payload_is_pos"]:
         np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64), pre["sorted_pos"])
     else:
-        bag = bag_of_position(wl)[pre["sorted_pos"]]
+        bag = bag_of_position(wl, pre["sorted_pos"])
         np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64), bag % wl.B)
     np.testing.assert_array_equal(res["unique_keys"].astype(np.int64), pre["unique_keys"])
     np.testing.assert_array_equal(res["seg_off"].astype(np.int64), pre["seg_off"])
@@ -162,12 +261,20 @@ def check_full(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, res: dict, p
     out, ab, oob, bad = oracle.forward(wl, wb, want_abs=True)
     assert_out_close(res["out"], out, ab, wl.dtype)
     assert int(res["status"][0]) == oob
+    malformed = oracle.offsets_check(wl)[0]
+    assert bool(res["status"][1] & 0x1) == malformed, "TBE_FLAG_BAD_OFFSETS"
     if res["path"] == 1:
         if pre is None:
             pre = oracle.preprocess(wl)
         check_inversion(wl, res, pre)
-    Wn, mn, U, _, _ = oracle.backward_adagrad(wl, wb, m0, G)
-    touched = touched_rows(wl)
+    Wn, mn, U, _, _, runs = oracle.backward_adagrad(wl, wb, m0, G, want_runs=True)
+    touched = np.zeros(wl.rows_total, bool)
+    touched[runs["keys"]] = True
+    if not malformed:
+        assert np.array_equal(touched, touched_rows(wl))
     assert U == int(touched.sum())
     assert_momentum_close(res["mom"], mn, m0, touched)
-    assert_weights_close(res["W"], Wn, wb, touched, wl.dtype)
+    k = runs["keys"]
+    arith = w_arith_bound(wl.dtype, runs["grad"], runs["abs"], runs["count"], m0[k],
+                          wvals_np(wb[k], wl.dtype), wl.lr, wl.eps, res["path"])
+    assert_weights_close(res["W"], Wn, wb, touched, wl.dtype, arith)

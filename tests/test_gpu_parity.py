@@ -36,7 +36,8 @@ def test_tiny_config():
 
 @pytest.mark.parametrize("pif", [True, False])
 def test_demo_config(pif):
-    _step(workloads.demo(B=1024), pif=pif)
+    # full size: T=16 tables of the demo list, B=4096 (~197K lookups)
+    _step(workloads.demo(), pif=pif)
 
 
 def test_mid_config_reduced_batch():
@@ -130,23 +131,103 @@ def test_empty_batch():
     assert res["num_unique"] == 0 and np.all(res["out"] == 0)
 
 
-def test_bad_offsets_flagged_and_treated_empty():
-    wl = workloads.make_workload("bad", T=1, table_rows=[50], D=16, dtype="f32", B=8,
-                                 lengths=("fixed", 4), dist=("uniform",), seed=1)
-    off = wl.offsets.copy()
-    off[3] = off[2] - 1          # bag 2 has end < start; bag 3 starts earlier
-    wl.offsets = off
-    from parity import device_batch
-    from recsys_table_embedding_gb300 import TBE, Tables
-    W = wl.weights().cuda()
-    tbe = TBE(Tables(W, wl.table_offset), device_batch(wl), preprocess_in_forward=False)
-    out = tbe.forward(device_batch(wl))
-    torch.cuda.synchronize()
-    st = tbe.status.cpu().numpy()
-    assert st[1] & 0x1
-    ref, _, _, bad = oracle.forward(wl, W.cpu().numpy())
-    assert bad == 1
-    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=1e-6, atol=0)
+def _malformed(pattern, dtype="f32", weighted=False):
+    """A batch whose offsets break the CSR rules in one way, with junk lookups
+    (in-range ones too) wherever a lookup belongs to no well-formed bag."""
+    wl = workloads.make_workload("bad", T=2, table_rows=[60, 300], D=16, dtype=dtype, B=40,
+                                 lengths=("poisson", 5.0), dist=("zipf", 1.1), seed=17,
+                                 weighted=[True, False] if weighted else None)
+    rng = np.random.default_rng(3)
+    off = wl.offsets.astype(np.int64)
+    idx = wl.indices
+    psw = wl.per_sample_weights
+    NB, N = wl.NB, wl.N
+
+    def junk(n):
+        return rng.integers(0, 60, size=n).astype(np.int32)
+
+    if pattern == "gap_before":
+        idx = np.concatenate([junk(9), idx])
+        off = off + 9
+        psw = None if psw is None else np.concatenate([np.ones(9, np.float32), psw])
+    elif pattern == "gap_after":
+        idx = np.concatenate([idx, junk(11)])
+        psw = None if psw is None else np.concatenate([psw, np.ones(11, np.float32)])
+    elif pattern == "start_negative":
+        off = off.copy()
+        off[0] = -3
+    elif pattern == "end_past_n":
+        off = off.copy()
+        off[NB] = N + 4
+    elif pattern == "end_below_start":
+        off = off.copy()
+        g = int(np.flatnonzero(np.diff(off) >= 3)[3])
+        off[g + 1] = off[g] - 2      # bag g malformed, bag g+1 overlaps bag g-1
+    wl.offsets = off.astype(np.int32)
+    wl.indices = idx.astype(np.int32)
+    wl.per_sample_weights = psw
+    return wl
+
+
+@pytest.mark.parametrize("pattern", ["gap_before", "gap_after", "start_negative", "end_past_n",
+                                     "end_below_start"])
+@pytest.mark.parametrize("pif", [True, False])
+@pytest.mark.parametrize("dtype,weighted", [("f32", False), ("bf16", True)])
+def test_malformed_offsets_forward_and_backward(pattern, pif, dtype, weighted):
+    # The metadata buffer starts as zero bytes (key 0 is a real row): a
+    # lookup position that no kernel rewrites would update row 0 or a row of
+    # a stale run.  The step must match the oracle, which ignores lookups
+    # outside well-formed bags and updates nothing when offsets decrease.
+    wl = _malformed(pattern, dtype, weighted)
+    assert oracle.offsets_check(wl)[0]
+    W0, G, m0 = wl.weights(), wl.grad_out(), _m0(wl)
+    res = run_cuda(wl, W0, G, m0, preprocess_in_forward=pif, meta_fill=0)
+    check_full(wl, W0, G, m0, res)
+    assert res["status"][1] & 0x1
+    if pattern == "end_below_start":
+        assert res["num_unique"] == 0
+        np.testing.assert_array_equal(res["mom"], m0)
+
+
+def test_fp32_tables_accumulate_in_fp64():
+    # Decision checklist item 1: FP64 accumulation for FP32 weights.  Values
+    # 1, 2^-30 and -1 sum to 2^-30 exactly in FP64; an FP32 accumulator that
+    # already holds a partial of magnitude >= 1 drops the 2^-30.
+    #   forward: bag (0,0) = 64 x row0 (1.0), row2 (2^-30), 64 x row3 (-1.0), row1 (0)
+    #   short run: row 1 of table 0 is looked up once by bags 0..128, whose
+    #              gradients are 1 (b < 64), 2^-30 (b = 64), -1 (b > 64)
+    #   long run:  row 0 of table 1 is looked up once by bags 0..300 (two
+    #              256-lookup chunks), gradients 1 (b < 150), 2^-30, -1 (b > 150)
+    tiny = 2.0 ** -30
+    D, B = 16, 301
+    lists = [[] for _ in range(2 * B)]
+    lists[0] = [0] * 64 + [2] + [3] * 64
+    for b in range(129):
+        lists[b].append(1)
+    for b in range(B):
+        lists[B + b].append(0)
+    lens = np.array([len(x) for x in lists])
+    wl = workloads.Workload(name="fp64", T=2, B=B, D=D, dtype="f32", table_rows=np.array([4, 2]),
+                            offsets=np.concatenate([[0], np.cumsum(lens)]).astype(np.int32),
+                            indices=np.concatenate([np.array(x, np.int32) for x in lists]),
+                            per_sample_weights=None, weighted_tables=None)
+    W0 = torch.zeros(6, D, dtype=torch.float32)
+    W0[0], W0[1], W0[2], W0[3] = 1.0, 0.0, tiny, -1.0
+    W0[4] = 0.005
+    W0[5] = -0.003
+    G = np.zeros((B, 2 * D), np.float32)
+    G[:64, :D], G[64, :D], G[65:129, :D] = 1.0, tiny, -1.0
+    G[:150, D:], G[150, D:], G[151:, D:] = 1.0, tiny, -1.0
+    m0 = np.zeros(6, np.float32)
+    # the test data: row gradients of both runs are 2^-30 exactly
+    _, _, _, rg, _ = oracle.backward_adagrad(wl, W0.numpy(), m0, G, want_row_grad=True)
+    assert np.all(rg[1] == tiny) and np.all(rg[4] == tiny)
+    res = run_cuda(wl, W0, G, m0)
+    assert res["num_long"] == 1
+    np.testing.assert_array_equal(res["out"][0, :D], np.full(D, tiny, np.float32))
+    check_full(wl, W0, G, m0, res)
+    # the update the 2^-30 gradient makes is far above FP32 noise
+    assert np.all(np.abs(res["W"][1]) > 1e-4) and np.all(np.abs(res["W"][4] - 0.005) > 1e-4)
 
 
 @pytest.mark.parametrize("B", [4096, 3000])
