@@ -131,22 +131,39 @@ def preprocess(wl):
                 seg_off=so[:U + 1], num_unique=int(U), n_valid=nv)
 
 
+def num_runs(wl) -> int:
+    """Number of runs (unique touched rows) of the batch inversion."""
+    L = lib()
+    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
+    return int(L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(idx), _p(off), wl.N, None, None, None,
+                                       None, None, None))
+
+
 def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarray,
                      want_row_grad: bool = False, want_update_count: bool = False,
-                     want_row_abs: bool = False):
+                     want_runs: bool = False):
     """Backward + exact rowwise Adagrad, in place on copies.
 
-    Returns (W_new, momentum_new, U, row_grad|None, update_count|None), plus
-    row_abs (the per-element sum of the row gradient's term magnitudes) as a
-    sixth item when ``want_row_abs``.
+    Returns (W_new, momentum_new, U, row_grad|None, update_count|None);
+    row_grad is dense [rows_total, D] (small problems only).  With
+    ``want_runs`` a sixth item is a dict of per-run arrays in ascending key
+    order: keys [U], grad [U, D] (the row gradient), abs [U, D] (the sum of
+    its terms' magnitudes) and count [U] (lookups of the run).
     """
     L = lib()
     W = _wbits(W, wl.dtype).copy()
     m = np.ascontiguousarray(momentum, dtype=np.float32).copy()
     to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
     go = np.ascontiguousarray(grad_out, dtype=np.float32)
-    rg = np.zeros((wl.rows_total, wl.D), np.float64) if want_row_grad else None
-    ra = np.zeros((wl.rows_total, wl.D), np.float64) if want_row_abs else None
+    runs = None
+    rg = ra = None
+    if want_row_grad or want_runs:
+        pre = preprocess(wl)
+        U0 = pre["num_unique"]
+        rg = np.zeros((max(U0, 1), wl.D), np.float64)
+        ra = np.zeros((max(U0, 1), wl.D), np.float64)
+        runs = dict(keys=pre["unique_keys"], grad=rg[:U0], abs=ra[:U0], count=pre["run_len"])
     uc = np.zeros(wl.rows_total, np.int32) if want_update_count else None
     # widened copies are held in locals: the C call reads them
     idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
@@ -154,9 +171,13 @@ def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarr
     U = L.tbe_oracle_backward_adagrad(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(m), _p(to),
                                       _p(idx), _p(off), wl.N, _p(psw), _p(wt), _p(go),
                                       float(wl.lr), float(wl.eps), _p(rg), _p(ra), _p(uc))
-    if want_row_abs:
-        return W, m, int(U), rg, uc, ra
-    return W, m, int(U), rg, uc
+    dense = None
+    if want_row_grad:
+        dense = np.zeros((wl.rows_total, wl.D), np.float64)
+        dense[runs["keys"]] = runs["grad"]
+    if want_runs:
+        return W, m, int(U), dense, uc, runs
+    return W, m, int(U), dense, uc
 
 
 def rows_update(wl, rows: np.ndarray, W_rows: np.ndarray, mom_rows: np.ndarray,

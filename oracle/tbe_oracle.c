@@ -388,10 +388,11 @@ static void adagrad_row(void *W, float *momentum, int32_t D, int32_t dtype, int6
  *     g[d] = sum_{p in run r, sorted order} w_p * grad_out[b(p), t*D + d]
  * and exactly one Adagrad update of that row.  W and momentum are updated in
  * place; rows no in-range lookup touches are not written.
- * row_grad (nullable, [rows_total, D]) receives g of every touched row;
- * row_abs (nullable, [rows_total, D]) receives sum |w_p * grad_out[..]| of
- * the same terms (the scale that bounds a summation-order rounding of g);
- * update_count (nullable, [rows_total]) counts updates applied per row.
+ * run_grad (nullable, [U, D]) receives g of run r (rows in ascending key
+ * order, the order of tbe_oracle_preprocess's unique_keys); run_abs
+ * (nullable, [U, D]) the sum |w_p * grad_out[..]| of the same terms (the
+ * scale that bounds a summation-order rounding of g); update_count
+ * (nullable, [rows_total]) counts updates applied per row.
  * Returns U, the number of rows updated.
  */
 int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dtype, void *W,
@@ -399,7 +400,7 @@ int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dty
                                     const int64_t *indices, const int64_t *offsets, int64_t N,
                                     const float *psw, const uint8_t *weighted,
                                     const float *grad_out, float lr, float eps,
-                                    double *row_grad, double *row_abs, int32_t *update_count)
+                                    double *run_grad, double *run_abs, int32_t *update_count)
 {
     int64_t *skeys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     int64_t *spos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
@@ -424,12 +425,12 @@ int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dty
                 ga[d] += fabs(w * (double)grow[d]);
             }
         }
-        if (row_grad)
+        if (run_grad)
             for (int d = 0; d < D; ++d)
-                row_grad[row * D + d] = g[d];
-        if (row_abs)
+                run_grad[r * D + d] = g[d];
+        if (run_abs)
             for (int d = 0; d < D; ++d)
-                row_abs[row * D + d] = ga[d];
+                run_abs[r * D + d] = ga[d];
         adagrad_row(W, momentum, D, dtype, row, g, lr, eps);
         if (update_count)
             update_count[row] += 1;
