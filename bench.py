@@ -54,6 +54,7 @@ def parse_args():
     ap.add_argument("--hist-mode", type=int, default=0, help="0 auto, 1 off, 2 force")
     ap.add_argument("--preprocess", default="config", choices=["config", "forward", "backward"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of CUDA graphs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip e2e, cpu baseline and clocks (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
@@ -144,24 +145,35 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def src_hash() -> str:
-    h = hashlib.sha256()
+KERNEL_SOURCE = [("tbe_fwd_", "forward.cu"), ("tbe_linearize", "forward.cu"),
+                 ("tbe_offsets_fixup", "forward.cu"), ("tbe_sort_", "sort.cu"), ("tbe_rle_", "rle.cu"),
+                 ("tbe_route", "rle.cu"), ("tbe_chunk_", "rle.cu"), ("tbe_zero_counters", "rle.cu"),
+                 ("tbe_bwd_", "backward.cu"), ("tbe_hist_", "hist.cu")]
+
+
+def src_hash(kernel: str):
+    """Hash of the source file that holds `kernel` and of the shared internal
+    header: an ncu summary is current only while both are unchanged."""
+    fn = next((f for pre, f in KERNEL_SOURCE if kernel.startswith(pre)), None)
+    if fn is None:
+        return None
     d = os.path.join(ROOT, "recsys_table_embedding_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    h = hashlib.sha256()
+    for f in (fn, "tbe_internal.cuh"):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, or None
-    when there is none or the kernel sources changed since it was taken."""
+    when there is none or the kernel's source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    h = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != src_hash():
+    h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != src_hash(kernel):
         return None
     return float(m.group(1))
 
@@ -222,6 +234,14 @@ def kernel_bytes(name: str, wl, st, pif: bool):
         return 4 * st.get("N_short", 0) + st.get("N_short", 0) * D * 4 + us * (2 * D * sw + 8 + 8)
     if name == "tbe_sort_onesweep":
         return 16 * N
+    if name in ("tbe_sort_histogram", "tbe_rle_count"):
+        return 4 * N
+    if name == "tbe_rle_write":
+        return 4 * N + 8 * st.get("U", 0)
+    if name == "tbe_linearize":
+        return 4 * N + 4 * (NB + 1) + 8 * N
+    if name == "tbe_bwd_apply":
+        return st.get("num_long", 0) * (2 * D * sw + 8)
     if name == "tbe_hist_fwd_umma":
         return 4 * N + 4 * (NB + 1) + NB * D * 4 + NB * 64 * 2
     if name == "tbe_hist_bwd_umma":
@@ -271,25 +291,75 @@ def run_ours(args):
     st = run_stats(wl, tbe)
     status = tbe.status.cpu().numpy()
 
-    # per-kernel CUDA events recorded by the library on this stream
+    # Per-kernel CUDA events recorded by the library around each of its
+    # launches on the step's stream; one set per timed step.  The span of a
+    # step (and of its forward and backward) runs from its first kernel's
+    # start event to its last kernel's end event.
     max_pairs = 64
-    per_call = []
-    for _ in range(2 * args.steps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_pairs)]
-        for e in evs:
-            e.record(stream)     # creates the CUDA event so its handle exists
-        handles = (ctypes.c_void_p * (2 * max_pairs))(*[e.cuda_event for e in evs])
-        names = (ctypes.c_char_p * max_pairs)()
-        used = ctypes.c_int32(0)
-        per_call.append((evs, handles, names, used))
-    torch.cuda.synchronize(dev)
 
-    def arm(i):
-        evs, handles, names, used = per_call[i]
-        cfg.kernel_events = ctypes.cast(handles, ctypes.c_void_p)
-        cfg.kernel_names = ctypes.cast(names, ctypes.c_void_p)
-        cfg.n_kernel_events = max_pairs
-        cfg.kernel_events_used = ctypes.cast(ctypes.pointer(used), ctypes.c_void_p)
+    class Slot:
+        def __init__(self):
+            self.evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_pairs)]
+            for e in self.evs:
+                e.record(stream)     # creates the CUDA event so its handle exists
+            self.handles = (ctypes.c_void_p * (2 * max_pairs))(*[e.cuda_event for e in self.evs])
+            self.names = (ctypes.c_char_p * max_pairs)()
+            self.used = ctypes.c_int32(0)
+            self.n_fwd = 0
+
+        def arm(self):
+            self.used.value = 0
+            cfg.kernel_events = ctypes.cast(self.handles, ctypes.c_void_p)
+            cfg.kernel_names = ctypes.cast(self.names, ctypes.c_void_p)
+            cfg.n_kernel_events = max_pairs
+            cfg.kernel_events_used = ctypes.cast(ctypes.pointer(self.used), ctypes.c_void_p)
+
+        def run(self, strm=None):
+            self.arm()
+            tbe.forward(batch, out, stream=strm)
+            self.n_fwd = self.used.value
+            tbe.backward(batch, mom, G, wl.lr, wl.eps, stream=strm)
+
+        def spans(self):
+            """(step, forward, backward) milliseconds and per-kernel (name, ms)."""
+            n = self.used.value
+            e = self.evs
+            kern = [(self.names[i].decode(), e[2 * i].elapsed_time(e[2 * i + 1])) for i in range(n)]
+            stp = e[0].elapsed_time(e[2 * n - 1])
+            fwd = e[0].elapsed_time(e[2 * self.n_fwd - 1])
+            bwd = e[2 * self.n_fwd].elapsed_time(e[2 * n - 1]) if n > self.n_fwd else 0.0
+            return stp, fwd, bwd, kern
+
+    def disarm():
+        cfg.kernel_events = None
+        cfg.kernel_events_used = None
+
+    # the timed steps run as CUDA graphs, one per step (each holds its own
+    # events), captured after the warm-up: replaying a graph enqueues the
+    # whole step at once, so the GPU never waits for the host between kernels
+    slots = [Slot() for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    graphs = []
+    mode = "cuda_graph"
+    if not args.eager:
+        try:
+            cap = torch.cuda.Stream(dev)
+            for sl in slots:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                    sl.run()
+                graphs.append(g)
+            disarm()
+            for g in graphs:          # upload and warm each graph once
+                g.replay()
+            torch.cuda.synchronize(dev)
+        except Exception as e:       # graphs are an optimisation of the timed loop only
+            disarm()
+            graphs = []
+            mode = f"eager (graph capture failed: {type(e).__name__}: {str(e)[:120]})"
+            torch.cuda.synchronize(dev)
+    else:
+        mode = "eager"
 
     clocks = ClockSampler(local) if not args.quick else None
     if world > 1:
@@ -300,31 +370,58 @@ def run_ours(args):
         time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
     t0.record(stream)
     for k in range(args.steps):
-        arm(2 * k)
-        tbe.forward(batch, out)
-        arm(2 * k + 1)
-        tbe.backward(batch, mom, G, wl.lr, wl.eps)
+        if graphs:
+            graphs[k].replay()
+        else:
+            slots[k].run()
     t1.record(stream)
+    host_ms = (time.perf_counter() - h0) * 1e3
     torch.cuda.synchronize(dev)
-    cfg.kernel_events = None
+    disarm()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
     ms_total = t0.elapsed_time(t1)
 
-    # per-kernel durations
+    # per-kernel durations and per-step spans
     kern = {}
     launches = 0
-    for evs, handles, names, used in per_call:
-        launches += used.value
-        for i in range(used.value):
-            nm = names[i].decode()
-            dt = evs[2 * i].elapsed_time(evs[2 * i + 1])
+    steps_ms, fwd_ms, bwd_ms = [], [], []
+    for sl in slots:
+        stp, fwd, bwd, kl = sl.spans()
+        steps_ms.append(stp)
+        fwd_ms.append(fwd)
+        bwd_ms.append(bwd)
+        launches += len(kl)
+        for nm, dt in kl:
             d = kern.setdefault(nm, [0, 0.0])
             d[0] += 1
             d[1] += dt
+    kern_sum = sum(v[1] for v in kern.values())
+
+    # the same steps launched one call at a time (no graph), for comparison:
+    # shows what host-side enqueueing costs the eager API
+    eager = None
+    if graphs and not args.quick:
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        h1 = time.perf_counter()
+        e0.record(stream)
+        for k in range(args.steps):
+            slots[k].run()
+        e1.record(stream)
+        eh = (time.perf_counter() - h1) * 1e3
+        torch.cuda.synchronize(dev)
+        disarm()
+        eks = sum(sum(dt for _, dt in sl.spans()[3]) for sl in slots)
+        et = e0.elapsed_time(e1)
+        eager = {"ms_per_step": round(et / args.steps, 4),
+                 "host_enqueue_ms_per_step": round(eh / args.steps, 4),
+                 "gpu_gap_ms_per_step": round((et - eks) / args.steps, 4)}
 
     ms_total = reduce_max(ms_total, dev, world)
     ms_step = ms_total / args.steps
@@ -351,16 +448,25 @@ def run_ours(args):
             roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                     "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
                     "traffic": traffic, "bytes_per_launch": kb,
-                    "avg_launch_ms": round(avg_s * 1e3, 4), "peak_source": peak_src}
+                    "avg_launch_ms": round(avg_s * 1e3, 4), "peak_source": peak_src,
+                    "frac_basis": "algorithmic bytes: each lookup's row read counted once, "
+                                  "re-reads that L2 serves included, so frac can exceed 1; "
+                                  "dram_frac is the HBM figure"}
             if traffic:
-                # what DRAM itself delivered: algorithmic bytes above count
-                # re-reads that L2 serves, so `frac` can exceed 1
+                # what DRAM itself delivered
                 dach = traffic / avg_s / 1e9
                 roof["dram_achieved"] = round(dach, 1)
                 roof["dram_frac"] = round(dach / hbm_peak, 4)
     step_ach = sb["total"] / (ms_step / 1e3) / 1e9
-    kernels = {n: {"launches": c, "avg_ms": round(t / c, 4), "share": round(t / sum(v[1] for v in kern.values()), 4)}
-               for n, (c, t) in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+    kernels = {}
+    for n, (c, t) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
+        kernels[n] = {"launches": c, "avg_ms": round(t / c, 4), "share": round(t / kern_sum, 4)}
+        kb_n = kernel_bytes(n, wl, st, pif)
+        if kb_n:
+            kernels[n]["algo_gbs"] = round(kb_n / (t / c / 1e3) / 1e9, 1)
+        tr = ncu_traffic(n, args.workload)
+        if tr:
+            kernels[n]["dram_gbs"] = round(tr / (t / c / 1e3) / 1e9, 1)
 
     res = None
     if rank == 0:
@@ -372,6 +478,13 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
+            "ms_per_step_median": round(float(np.median(steps_ms)), 4),
+            "forward_ms_median": round(float(np.median(fwd_ms)), 4),
+            "backward_ms_median": round(float(np.median(bwd_ms)), 4),
+            "launch_mode": mode,
+            "host_enqueue_ms_per_step": round(host_ms / args.steps, 4),
+            "gpu_gap_ms_per_step": round((ms_total - kern_sum) / args.steps, 4),
+            "eager": eager,
             "config": {"workload": wl.name + ": " + wl.desc,
                        "weights": wl.dtype, "accumulate": "f64" if wl.dtype == "f32" else "f32",
                        "preprocess_in_forward": pif, "path": "histogram" if tbe.path == 2 else "generic",

@@ -978,11 +978,8 @@ size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype) {
 }
 
 template <typename K>
-static int persistent_grid(K kernel, int num_sms, size_t smem = 0, int threads = 256) {
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
-    if (per_sm < 1) per_sm = 1;
-    return num_sms * per_sm;
+static int persistent_grid(const Launch &L, K kernel, size_t smem = 0, int threads = 256) {
+    return L.num_sms * cached_blocks_per_sm(L.dev, (const void *)kernel, threads, smem);
 }
 
 static constexpr bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -998,19 +995,15 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
     const size_t csm = (size_t)(CHUNK_THREADS / 32) * warp_smem_bytes(p.chunk);
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, false>;
-        cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
-        cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+        cached_smem_attr(L.dev, (const void *)kc, csm);
         L.before("tbe_bwd_grad_accum");
-        kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
+        kc<<<persistent_grid(L, kc, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     } else {
         auto kc = tbe_bwd_chunk_kernel<WT, LPR, NV, true>;
-        cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
-        cudaFuncSetAttribute(kc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+        cached_smem_attr(L.dev, (const void *)kc, csm);
         L.before("tbe_bwd_fused_long");
-        kc<<<persistent_grid(kc, L.num_sms, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
+        kc<<<persistent_grid(L, kc, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
         L.after();
     }
     bool stream = false;
@@ -1024,11 +1017,9 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         // on the large one)
         auto ks = tbe_bwd_short_stream_kernel<WT, NV>;
         const size_t ssm = (size_t)SS_WARPS * ss_warp_bytes();
-        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
-        cudaFuncSetAttribute(ks, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+        cached_smem_attr(L.dev, (const void *)ks, ssm);
         L.before("tbe_bwd_short_run");
-        ks<<<persistent_grid(ks, L.num_sms, ssm, SS_WARPS * 32), SS_WARPS * 32, ssm, L.stream>>>(p);
+        ks<<<persistent_grid(L, ks, ssm, SS_WARPS * 32), SS_WARPS * 32, ssm, L.stream>>>(p);
         L.after();
     }
     if (!stream) {
@@ -1040,13 +1031,13 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         constexpr int SU = SNV >= 3 ? 2 : 4;
         auto ks = tbe_bwd_short_kernel<WT, SGL, SNV, SU>;
         L.before("tbe_bwd_short_run");
-        ks<<<persistent_grid(ks, L.num_sms), 256, 0, L.stream>>>(p);
+        ks<<<persistent_grid(L, ks), 256, 0, L.stream>>>(p);
         L.after();
     }
     if (long_mode == TBE_LONG_TWO_KERNEL) {
         auto ka = tbe_bwd_apply_kernel<WT, LPR, NV>;
         L.before("tbe_bwd_apply");
-        ka<<<persistent_grid(ka, L.num_sms), 256, 0, L.stream>>>(p);
+        ka<<<persistent_grid(L, ka), 256, 0, L.stream>>>(p);
         L.after();
     }
 }

@@ -308,12 +308,10 @@ RowPlan row_plan(int D, int bytes_per_elem) {
 }
 
 template <typename K>
-static int grid_for(K kernel, int threads, int64_t work_warps, int num_sms) {
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
-    if (per_sm < 1) per_sm = 1;
+static int grid_for(const Launch &L, K kernel, int threads, int64_t work_warps) {
+    const int per_sm = cached_blocks_per_sm(L.dev, (const void *)kernel, threads, 0);
     const int64_t want = (work_warps * 32 + threads - 1) / threads;
-    int64_t g = (int64_t)num_sms * per_sm;
+    int64_t g = (int64_t)L.num_sms * per_sm;
     if (want < g) g = want;
     return (int)(g < 1 ? 1 : g);
 }
@@ -343,7 +341,7 @@ static void fwd_launch(Launch &L, const FwdParams &p) {
     auto k = p.psw != nullptr
                  ? (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, true> : tbe_fwd_kernel<WT, VB, LPR, NV, US, true>)
                  : (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false> : tbe_fwd_kernel<WT, VB, LPR, NV, US, false>);
-    const int grid = grid_for(k, 256, p.NB, L.num_sms);
+    const int grid = grid_for(L, k, 256, p.NB);
     L.before("tbe_fwd_gather");
     k<<<grid, 256, 0, L.stream>>>(p);
     L.after();
@@ -415,7 +413,7 @@ tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *b
                             int32_t *counters) {
     FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
-    const int grid = grid_for(tbe_linearize_kernel, 256, p.NB, L.num_sms);
+    const int grid = grid_for(L, tbe_linearize_kernel, 256, p.NB);
     L.before("tbe_linearize");
     tbe_linearize_kernel<<<grid, 256, 0, L.stream>>>(p);
     L.after();

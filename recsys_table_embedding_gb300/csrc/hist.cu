@@ -663,9 +663,7 @@ static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_ba
     p.tiles_total = p.tiles_per_table * tab->T;
     p.do_mma = do_mma;
     const size_t smem = fwd_smem();
-    cudaFuncSetAttribute(tbe_hist_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(tbe_hist_fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+    cached_smem_attr(L.dev, (const void *)tbe_hist_fwd_kernel, smem);
     // CTAs per SM: shared memory (227 KB usable, 1 KB reserved per CTA) and
     // TMEM (512 columns, 128 per CTA) both allow 4 (64 registers x 256 threads allow 4)
     int per_sm = (int)((227 * 1024) / (smem + 1024));
@@ -723,9 +721,7 @@ tbe_status launch_hist_backward(Launch &L, const tbe_tables *tab, const tbe_batc
     hist_zero_kernel<<<1, 256, 0, L.stream>>>(p.arrive, tab->T);
     L.after();
     const size_t smem = bwd_smem();
-    cudaFuncSetAttribute(tbe_hist_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(tbe_hist_bwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+    cached_smem_attr(L.dev, (const void *)tbe_hist_bwd_kernel, smem);
     L.before("tbe_hist_bwd_umma");
     tbe_hist_bwd_kernel<<<(unsigned)(tab->T * p.S), HB_THREADS, smem, L.stream>>>(p);
     L.after();

@@ -312,10 +312,7 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
 
     const size_t smem = sizeof(PassSmem);
     static_assert(sizeof(PassSmem) < 227 * 1024, "pass shared memory");
-    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel, smem);
     const uint32_t *ki = keys_a, *vi = vals_a;
     uint32_t *ko = keys_b, *vo = vals_b;
     for (int ps = 0; ps < passes; ++ps) {
@@ -366,8 +363,7 @@ tbe_status launch_sort_selftest(Launch &L, void *ws, int32_t *status) {
     sort_selftest_init_kernel<<<8, 256, 0, L.stream>>>(w, words, ticket);
     L.after();
     const size_t smem = sizeof(PassSmem);
-    cudaFuncSetAttribute(radix_onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
+    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel, smem);
     L.before("tbe_sort_onesweep");
     radix_onesweep_kernel<<<1, SORT_THREADS, smem, L.stream>>>(keys_in, vals_in, keys_out, vals_out,
                                                                 SELFTEST_N, 0, RADIX - 1, bucket,

@@ -4,29 +4,89 @@
 // stream; no device memory is allocated and no host synchronisation happens.
 #include <string.h>
 
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 
 #include "tbe_internal.cuh"
 
 namespace tbe {
 
+static int device_sms(int dev);
+
 Launch::Launch(cudaStream_t s, const tbe_config *c) : stream(s), cfg(c) {
     // event recording continues after the pairs earlier calls recorded
     if (cfg != nullptr && cfg->kernel_events_used != nullptr) used = *cfg->kernel_events_used;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    num_sms = device_sms(dev);
+    if (cfg != nullptr && cfg->kernel_events != nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        capturing = cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
+                    cs == cudaStreamCaptureStatusActive;
+    }
+}
+
+// Timing events: during stream capture an event record must be an external
+// event node of the graph (a plain record there only orders streams), so the
+// graph records the timestamps each time it runs.
+static void record(cudaEvent_t ev, cudaStream_t s, bool capturing) {
+    if (capturing) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else cudaEventRecord(ev, s);
 }
 
 void Launch::before(const char *name) {
     if (cfg == nullptr || cfg->kernel_events == nullptr || used >= cfg->n_kernel_events) return;
-    cudaEventRecord(cfg->kernel_events[2 * used], stream);
+    record(cfg->kernel_events[2 * used], stream, capturing);
     if (cfg->kernel_names != nullptr) cfg->kernel_names[used] = name;
 }
 
 void Launch::after() {
     if (cudaPeekAtLastError() != cudaSuccess) failed = true;
     if (cfg == nullptr || cfg->kernel_events == nullptr || used >= cfg->n_kernel_events) return;
-    cudaEventRecord(cfg->kernel_events[2 * used + 1], stream);
+    record(cfg->kernel_events[2 * used + 1], stream, capturing);
     ++used;
     if (cfg->kernel_events_used != nullptr) *cfg->kernel_events_used = used;
+}
+
+// ---- per-device caches of launch properties
+static std::mutex g_launch_mu;
+static std::map<int, int> g_sms;
+static std::map<std::tuple<int, const void *, int, size_t>, int> g_blocks;
+static std::set<std::tuple<int, const void *, size_t>> g_smem;
+
+static int device_sms(int dev) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n < 1) n = 1;
+    g_sms[dev] = n;
+    return n;
+}
+
+int cached_blocks_per_sm(int dev, const void *fn, int threads, size_t smem) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    const auto key = std::make_tuple(dev, fn, threads, smem);
+    auto it = g_blocks.find(key);
+    if (it != g_blocks.end()) return it->second;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess)
+        per_sm = 0;
+    if (per_sm < 1) per_sm = 1;
+    g_blocks[key] = per_sm;
+    return per_sm;
+}
+
+void cached_smem_attr(int dev, const void *fn, size_t smem) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    const auto key = std::make_tuple(dev, fn, smem);
+    if (g_smem.count(key)) return;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    g_smem.insert(key);
 }
 
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -186,13 +246,6 @@ static tbe_status check_meta(const tbe_meta *meta, const Problem &pr) {
     return TBE_OK;
 }
 
-static int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
-
 static tbe_status finish(const Launch &L, tbe_status st) {
     if (st != TBE_OK) return st;
     return L.failed ? TBE_ERR_CUDA : TBE_OK;
@@ -328,7 +381,6 @@ tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *
         if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
     }
     Launch L(stream, cfg);
-    L.num_sms = sm_count();
     if (meta != nullptr) launch_zero_counters(L, meta->counters);
     if (pr.path == 2) {
         st = launch_hist_forward(L, tables, batch, out, meta ? meta->hist : nullptr, dev_status,
@@ -353,7 +405,6 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
     if ((st = check_meta(meta, pr)) != TBE_OK) return st;
     if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
     Launch L(stream, cfg);
-    L.num_sms = sm_count();
     launch_zero_counters(L, meta->counters);
     if (pr.path == 2)
         return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status, meta->counters));
@@ -379,7 +430,6 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
     if ((st = check_meta(meta, pr)) != TBE_OK) return st;
     if (workspace_bytes < workspace_size(tables, batch, pr)) return TBE_ERR_BUFFER_TOO_SMALL;
     Launch L(stream, cfg);
-    L.num_sms = sm_count();
     if (pr.path == 2)
         return finish(L, launch_hist_backward(L, tables, batch, meta->hist, momentum, grad_out, lr,
                                               eps, workspace, dev_status, meta->counters));
@@ -433,7 +483,6 @@ tbe_status tbe_selftest_wait_limit(int32_t kind, void *workspace, size_t workspa
     if (kind != TBE_SELFTEST_SORT_LOOKBACK && kind != TBE_SELFTEST_COPY_WAIT)
         return TBE_ERR_INVALID_ARGUMENT;
     Launch L(stream, nullptr);
-    L.num_sms = sm_count();
     if (kind == TBE_SELFTEST_COPY_WAIT) return finish(L, launch_copy_wait_selftest(L, dev_status));
     if (workspace == nullptr) return TBE_ERR_NULL_POINTER;
     if (!aligned(workspace, 256)) return TBE_ERR_MISALIGNED;
@@ -500,7 +549,6 @@ extern "C" tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_
     if (rle_workspace_bytes(pr.N) > need) need = rle_workspace_bytes(pr.N);
     if (need > STATIC_SCRATCH_BYTES) return TBE_ERR_SCRATCH_LIMIT;
     Launch L(stream, cfg);
-    L.num_sms = sm_count();
     launch_zero_counters(L, meta->counters);
     // the histogram path's counting needs no scratch
     if (pr.path == 2)

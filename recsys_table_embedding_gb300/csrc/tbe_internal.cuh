@@ -122,12 +122,22 @@ struct Launch {
     cudaStream_t stream;
     const tbe_config *cfg;
     int used = 0;
+    int dev = 0;         // current device when the entry point was called
     int num_sms = 0;
+    bool capturing = false;   // `stream` is being captured into a CUDA graph
     bool failed = false;
     Launch(cudaStream_t s, const tbe_config *c);
     void before(const char *name);
     void after();
 };
+
+// Launch properties are looked up once per (device, kernel) and cached, so a
+// call enqueues its kernels without per-launch driver queries:
+// resident blocks per SM for `threads` threads and `smem` dynamic bytes ...
+int cached_blocks_per_sm(int dev, const void *fn, int threads, size_t smem);
+// ... and the dynamic shared-memory limit (with the max-shared carveout),
+// raised to `smem` bytes the first time a kernel needs it on a device.
+void cached_smem_attr(int dev, const void *fn, size_t smem);
 
 // Row-vector plan for a D-element row of `bytes_per_elem`: lanes per row
 // (LPR) and 16-byte vectors per lane (NV), with LPR * NV * 16 = row bytes.
