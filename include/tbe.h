@@ -71,7 +71,7 @@ typedef enum tbe_status {
     TBE_ERR_UNSUPPORTED_DIM = 3,    /* D*sizeof(weight) not one of the supported row sizes */
     TBE_ERR_UNSUPPORTED_DTYPE = 4,
     TBE_ERR_MISALIGNED = 5,         /* a device pointer is not 16-byte aligned */
-    TBE_ERR_KEY_RANGE = 6,          /* sum of E_t (+1 sentinel) does not fit int32 keys */
+    TBE_ERR_KEY_RANGE = 6,          /* sum of E_t is 2^62 or more */
     TBE_ERR_BUFFER_TOO_SMALL = 7,   /* workspace or meta smaller than tbe_query_sizes says */
     TBE_ERR_META = 8,               /* meta not bound, or bound for another problem */
     TBE_ERR_HISTOGRAM_SHAPE = 9,    /* histogram path forced on a shape it does not cover */
@@ -125,6 +125,10 @@ typedef struct tbe_config {
     const char **kernel_names;
     int32_t n_kernel_events;
     int32_t *kernel_events_used;
+    /* Width of the linearised keys: 0 = automatic (4 bytes while rows_total
+     * < 2^31 - 1, else 8), 8 = 64-bit keys for any problem (the wide path
+     * on small tables, e.g. to test it).  4 is accepted where 0 would pick it. */
+    int32_t key_bytes;
 } tbe_config;
 
 /* The tables: all T tables stored back to back in one [rows_total, D] array. */
@@ -137,15 +141,22 @@ typedef struct tbe_tables {
     int32_t dtype;                      /* tbe_dtype */
 } tbe_tables;
 
+/* Element type of a batch's indices and offsets (decision checklist item 6:
+ * int32 where the range allows, int64 otherwise; KeyedJagged tensors often
+ * carry int64). */
+typedef enum tbe_index_type { TBE_INDEX_I32 = 0, TBE_INDEX_I64 = 1 } tbe_index_type;
+
 /* One batch in KeyedJagged CSR form. */
 typedef struct tbe_batch {
-    const int32_t *indices;             /* device, [N]; row index within its table */
-    const int32_t *offsets;             /* device, [T*B+1]; offsets[0] = 0, offsets[T*B] = N */
+    const void *indices;                /* device, [N] of index_type; row index within its table */
+    const void *offsets;                /* device, [T*B+1] of index_type; offsets[0] = 0,
+                                           offsets[T*B] = N */
     int64_t N;                          /* number of lookups, 0 <= N < 2^30 */
     int64_t B;                          /* bags per table */
     const float *per_sample_weights;    /* device, [N] or NULL (unweighted) */
     const uint8_t *weighted_tables;     /* device, [T] or NULL: nonzero = table uses the weights;
                                            NULL with weights given = every table weighted */
+    int32_t index_type;                 /* tbe_index_type of indices and offsets */
 } tbe_batch;
 
 /*
@@ -154,9 +165,13 @@ typedef struct tbe_batch {
  * (when given a meta) or tbe_preprocess, consumed by the backward.  Bind it to
  * a caller device buffer with tbe_meta_bind; the fields are device pointers
  * into that buffer plus the problem it was bound for, and are read-only to
- * the caller.  After a generic-path forward/preprocess, on the device:
+ * the caller.  Linearised keys are uint32 (key_bytes = 4) when rows_total
+ * is below 2^31 - 1, uint64 (key_bytes = 8) otherwise (decision checklist
+ * item 6: int32 keys while the linearised range fits).  After a generic-path
+ * forward/preprocess, on the device:
  *   sorted_keys[0..N)  linearised keys table_offset[t]+idx in ascending order,
- *                      out-of-range lookups last with key = rows_total
+ *                      out-of-range lookups and lookups outside every
+ *                      well-formed bag last with key = rows_total
  *   sorted_vals[0..N)  payload in the same (stable) order: the bag index b
  *                      within its table when the batch is unweighted, else
  *                      the lookup position p (bag_of[p] then gives t*B+b)
@@ -171,10 +186,16 @@ typedef struct tbe_meta {
     int32_t bound_T, path;              /* path: 1 = generic, 2 = histogram */
     int32_t payload_is_pos, key_bits;
     int64_t rows_total;
-    uint32_t *sorted_keys, *sorted_vals;
-    uint32_t *keys_a, *vals_a, *keys_b, *vals_b;
+    int32_t key_bytes;                  /* 4 (uint32 keys) or 8 (uint64 keys) */
+    int32_t index_type;                 /* the batch's tbe_index_type */
+    void *sorted_keys;                  /* key arrays hold key_bytes per key */
+    uint32_t *sorted_vals;
+    void *keys_a;
+    uint32_t *vals_a;
+    void *keys_b;
+    uint32_t *vals_b;
     int32_t *bag_of;
-    uint32_t *unique_keys;
+    void *unique_keys;
     int32_t *seg_off;
     int32_t *counters;
     int32_t *long_run;                  /* [max_long] run id of long run l */
@@ -185,8 +206,8 @@ typedef struct tbe_meta {
                                            scratch otherwise, and slot c is taken c-th */
     int32_t *arrive;                    /* [max_long] arrival counters of the fused long-run path */
     int32_t *chunk_desc;                /* [max_chunks][8] per chunk slot: first and end sorted
-                                           position, key, table, long run, first slot of the run,
-                                           chunks of the run, window key */
+                                           position, key (low and high 32 bits), long run, first
+                                           slot of the run, chunks of the run, window key */
     uint16_t *hist;
     size_t bytes;
 } tbe_meta;

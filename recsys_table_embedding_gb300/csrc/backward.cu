@@ -45,7 +45,8 @@ struct BwdParams {
     const int32_t *bag_of;
     const float *psw;
     const uint8_t *weighted;
-    const uint32_t *unique_keys;
+    const void *unique_keys;      // uint32 or uint64 (key64)
+    int key64;
     const int32_t *seg_off;
     const int32_t *counters;
     const int32_t *long_run;
@@ -64,6 +65,12 @@ struct BwdParams {
     int chunk;
     int payload_pos;
 };
+
+// unique key r (a row of the weight array)
+__device__ __forceinline__ int64_t load_key(const BwdParams &p, int64_t r) {
+    return p.key64 ? (int64_t)__ldg(reinterpret_cast<const unsigned long long *>(p.unique_keys) + r)
+                   : (int64_t)__ldg(reinterpret_cast<const uint32_t *>(p.unique_keys) + r);
+}
 
 __device__ __forceinline__ void acc4(double (&a)[4], const float4 x, float w) {
     a[0] = fma((double)w, (double)x.x, a[0]);
@@ -207,7 +214,7 @@ __host__ __device__ constexpr int warp_smem_bytes(int chunk) {
 // One chunk of a long run, as the route kernel describes it.
 struct Chunk {
     int32_t s, e;      // sorted positions [s, e)
-    uint32_t key;
+    int64_t key;
     int t, l, cb, nch; // table, long run, its first chunk slot and chunk count
     int slot;          // chunk slot (index of its descriptor and its partial)
 };
@@ -218,7 +225,9 @@ __device__ __forceinline__ Chunk load_chunk(const BwdParams &p, int ci) {
     const int4 a = __ldg(reinterpret_cast<const int4 *>(p.chunk_desc) + 2 * (int64_t)slot);
     const int4 b = __ldg(reinterpret_cast<const int4 *>(p.chunk_desc) + 2 * (int64_t)slot + 1);
     Chunk c;
-    c.s = a.x; c.e = a.y; c.key = (uint32_t)a.z; c.t = a.w;
+    c.s = a.x; c.e = a.y;
+    c.key = (int64_t)(((uint64_t)(uint32_t)a.w << 32) | (uint32_t)a.z);
+    c.t = table_of_key(p.table_offset, p.T, c.key);
     c.l = b.x; c.cb = b.y; c.nch = b.z;
     c.slot = slot;
     return c;
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
         if (r < U_runs) {
             s = __ldg(p.seg_off + r);
             e = __ldg(p.seg_off + r + 1);
-            key = __ldg(p.unique_keys + r);
+            key = load_key(p, r);
         }
         const bool mine = r < U_runs && e - s < p.sl_threshold;
         ACC acc[NV][4];
@@ -657,7 +666,7 @@ struct SsTask {
     int nr;         // runs in the task
     int32_t s;      // first sorted position of the lane's run
     int32_t e;
-    uint32_t key;
+    int64_t key;
     int len;        // lookups of the lane's run if short, else 0
     int pre;        // exclusive prefix of len over the lanes
     int total;      // short-run lookups of the task
@@ -707,7 +716,7 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
         if (lane < T.nr) {
             T.s = __ldg(p.seg_off + q * RT + lane);
             T.e = __ldg(p.seg_off + q * RT + lane + 1);
-            T.key = __ldg(p.unique_keys + q * RT + lane);
+            T.key = load_key(p, (int64_t)q * RT + lane);
         }
     };
     // phase B: lengths of the short runs, prefixes, tables, momentum; the
@@ -903,7 +912,7 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
 #pragma unroll
                 for (int sh = 1; sh < 32; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
                 const float m_old = __shfl_sync(FULL, cur.mom, slot);
-                const uint32_t key = __shfl_sync(FULL, cur.key, slot);
+                const int64_t key = __shfl_sync(FULL, cur.key, slot);
                 const float m_new = A::mom(m_old, ss, p.D);
                 const auto den = A::den(m_new, p.eps);
                 const WT *wsrc = reinterpret_cast<const WT *>(wbuf + cw * SS_WBUF + slot * wrow) + lane * 4;
@@ -957,7 +966,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
         const int cb = __ldg(p.long_chunk_base + l);
         const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
         const int nch = (re - rs + p.chunk - 1) / p.chunk;
-        const int64_t key = __ldg(p.unique_keys + r);
+        const int64_t key = load_key(p, r);
         ACC acc[NV][4];
 #pragma unroll
         for (int q = 0; q < NV; ++q)
@@ -1070,6 +1079,7 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.psw = a.bt->per_sample_weights;
     p.weighted = a.bt->weighted_tables;
     p.unique_keys = m->unique_keys;
+    p.key64 = m->key_bytes == 8;
     p.seg_off = m->seg_off;
     p.counters = m->counters;
     p.long_run = m->long_run;

@@ -15,7 +15,10 @@
 // before accumulating.  Sub-group partial sums are combined with shuffles and
 // the pooled row is written once.  When preprocessing runs in the forward,
 // the same pass writes the linearised key and the sort payload of every
-// lookup (coalesced, in position order).
+// lookup (coalesced, in position order).  Indices and offsets are int32 or
+// int64 (kernels templated on the index type IdxT); keys are written here
+// only when they are 32-bit, the 64-bit keys of row ranges of 2^31 and more
+// come from the linearize kernel.
 #include <type_traits>
 
 #include "tbe_internal.cuh"
@@ -25,12 +28,12 @@ namespace tbe {
 struct FwdParams {
     const void *W;
     const int64_t *table_offset;
-    const int32_t *indices;
-    const int32_t *offsets;
+    const void *indices;   // IdxT [N]
+    const void *offsets;   // IdxT [NB+1]
     const float *psw;
     const uint8_t *weighted;
     float *out;
-    uint32_t *keys;
+    void *keys;            // KeyT [N] (uint32 in the forward kernel)
     uint32_t *vals;
     int32_t *bag_of;
     int32_t *status;
@@ -40,7 +43,7 @@ struct FwdParams {
     int64_t N;
     int T;
     int D;
-    uint32_t sentinel;
+    uint64_t sentinel;
     int payload_pos;
 };
 
@@ -92,24 +95,34 @@ template <int VEC, typename ACC> __device__ __forceinline__ void store_out(float
     }
 }
 
-// Well-formed bag: 0 <= start <= end <= N.  A malformed bag is made empty,
-// flagged in the status word and recorded in the counters (if any).
-__device__ __forceinline__ void check_bag(const FwdParams &p, int lane, int32_t &start, int32_t &end) {
-    if (start <= end && start >= 0 && (int64_t)end <= p.N) return;
+template <typename IdxT> __device__ __forceinline__ int64_t ld_off(const FwdParams &p, int64_t g) {
+    return (int64_t)__ldg(reinterpret_cast<const IdxT *>(p.offsets) + g);
+}
+
+// Lookup range of bag g.  Well-formed: 0 <= start <= end <= N; a malformed
+// bag is made empty, flagged in the status word and recorded in the
+// counters (if any).
+template <typename IdxT>
+__device__ __forceinline__ void read_bag(const FwdParams &p, int64_t g, int lane, int32_t &start,
+                                         int32_t &end) {
+    const int64_t s = ld_off<IdxT>(p, g), e = ld_off<IdxT>(p, g + 1);
+    start = (int32_t)s;
+    end = (int32_t)e;
+    if (s <= e && s >= 0 && e <= p.N) return;
     if (lane == 0) {
         atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
         if (p.counters != nullptr) {
             p.counters[C_MALFORMED] = 1;
-            if (end < start) p.counters[C_DECREASING] = 1;
+            if (e < s) p.counters[C_DECREASING] = 1;
         }
     }
     start = end = 0;
 }
 
 // offsets[0] != 0 or offsets[T*B] != N leaves lookups outside every bag
-__device__ __forceinline__ void check_span(const FwdParams &p) {
+template <typename IdxT> __device__ __forceinline__ void check_span(const FwdParams &p) {
     if (blockIdx.x != 0 || threadIdx.x != 0) return;
-    if (__ldg(p.offsets) != 0 || (int64_t)__ldg(p.offsets + p.NB) != p.N) {
+    if (ld_off<IdxT>(p, 0) != 0 || ld_off<IdxT>(p, p.NB) != p.N) {
         atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
         if (p.counters != nullptr) p.counters[C_MALFORMED] = 1;
     }
@@ -126,7 +139,7 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 // without predicates or branches; the rest of a 32-lookup block (and any
 // block with an out-of-range index) goes one 32/LPR-row step at a time with
 // per-row checks.  (t, b) of the next bag are stepped, not divided.
-template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED>
+template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED, typename IdxT>
 __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     constexpr int VEC = VB / (int)sizeof(WT);   // elements per lane vector
@@ -140,13 +153,14 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
     const int tstep = (int)(nwarps / p.B);
     const int64_t bstep = nwarps - (int64_t)tstep * p.B;
     int oob = 0;
-    check_span(p);
+    check_span<IdxT>(p);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(p.keys);
+    const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
     for (; bag < p.NB; bag += nwarps) {
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
-        int32_t start = __ldg(p.offsets + bag);
-        int32_t end = __ldg(p.offsets + bag + 1);
-        check_bag(p, lane, start, end);
+        int32_t start, end;
+        read_bag<IdxT>(p, bag, lane, start, end);
         const bool wt = WEIGHTED && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         const WT *Wt = reinterpret_cast<const WT *>(p.W) + row0 * p.D + li * VEC;
         ACC acc[NV][VEC];
@@ -157,16 +171,16 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
 
         for (int32_t base = start; base < end; base += 32) {
             const int n = min(32, end - base);
-            int32_t idx = 0;
+            IdxT idx = 0;
             float w = 1.f;
             if (lane < n) {
-                idx = __ldg(p.indices + base + lane);
+                idx = __ldg(indices + base + lane);
                 if (wt) w = __ldg(p.psw + base + lane);
             }
             const bool valid = lane < n && idx >= 0 && (int64_t)idx < E;
             oob += (lane < n) && !valid;
-            if (p.keys != nullptr && lane < n) {
-                p.keys[base + lane] = valid ? (uint32_t)(row0 + idx) : p.sentinel;
+            if (keys != nullptr && lane < n) {
+                keys[base + lane] = valid ? (uint32_t)(row0 + idx) : (uint32_t)p.sentinel;
                 p.vals[base + lane] = p.payload_pos ? (uint32_t)(base + lane) : (uint32_t)b;
                 if (p.bag_of != nullptr) p.bag_of[base + lane] = (int32_t)bag;
             }
@@ -179,7 +193,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
                     float wv[U];
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const int32_t ik = __shfl_sync(FULL, idx, j + u * RPI + sub);
+                        const IdxT ik = __shfl_sync(FULL, idx, j + u * RPI + sub);
                         wv[u] = WEIGHTED ? __shfl_sync(FULL, w, j + u * RPI + sub) : 1.f;
                         const WT *r = Wt + (int64_t)ik * p.D;
 #pragma unroll
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
             for (; j < n; j += RPI) {
                 const int k = j + sub;
                 const int src = k & 31;
-                const int32_t ik = __shfl_sync(FULL, idx, src);
+                const IdxT ik = __shfl_sync(FULL, idx, src);
                 const float wk = WEIGHTED ? __shfl_sync(FULL, w, src) : 1.f;
                 if (k < n && ((vmask >> src) & 1u)) {
                     const WT *r = Wt + (int64_t)ik * p.D;
@@ -230,25 +244,28 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
 }
 
 // Linearize alone (the batch inversion's first step when it runs at the
-// start of the backward): one warp per bag writes key and payload of every
-// lookup; out-of-range lookups get the sentinel key (the forward counts them).
+// start of the backward, or when keys are 64-bit): one warp per bag writes
+// key and payload of every lookup; out-of-range lookups get the sentinel key
+// (the forward counts them).
+template <typename IdxT, typename KeyT>
 __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    check_span(p);
+    check_span<IdxT>(p);
+    KeyT *keys = reinterpret_cast<KeyT *>(p.keys);
+    const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
     for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < p.NB;
          bag += nwarps) {
         const int t = (int)(bag / p.B);
         const int64_t b = bag - (int64_t)t * p.B;
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
-        int32_t start = __ldg(p.offsets + bag);
-        int32_t end = __ldg(p.offsets + bag + 1);
-        check_bag(p, lane, start, end);
+        int32_t start, end;
+        read_bag<IdxT>(p, bag, lane, start, end);
         for (int32_t i = start + lane; i < end; i += 32) {
-            const int32_t idx = __ldg(p.indices + i);
+            const IdxT idx = __ldg(indices + i);
             const bool valid = idx >= 0 && (int64_t)idx < E;
-            p.keys[i] = valid ? (uint32_t)(row0 + idx) : p.sentinel;
+            keys[i] = valid ? (KeyT)(row0 + idx) : (KeyT)p.sentinel;
             p.vals[i] = p.payload_pos ? (uint32_t)i : (uint32_t)b;
             if (p.bag_of != nullptr) p.bag_of[i] = (int32_t)bag;
         }
@@ -263,8 +280,10 @@ __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
 // last and no run starts at it), payload 0 and bag -1.  When some bag ends
 // before it starts, two well-formed bags can hold one lookup, and every
 // lookup gets the sentinel: such a batch has no backward update.
+template <typename IdxT, typename KeyT>
 __global__ void __launch_bounds__(256) tbe_offsets_fixup_kernel(const FwdParams p) {
     if (__ldg(p.counters + C_MALFORMED) == 0) return;
+    KeyT *keys = reinterpret_cast<KeyT *>(p.keys);
     const bool decreasing = __ldg(p.counters + C_DECREASING) != 0;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.N; i += stride) {
@@ -274,14 +293,13 @@ __global__ void __launch_bounds__(256) tbe_offsets_fixup_kernel(const FwdParams 
             int64_t lo = 0, hi = p.NB + 1;   // answer in [lo - 1, hi)
             while (lo < hi) {
                 const int64_t mid = (lo + hi) >> 1;
-                if ((int64_t)__ldg(p.offsets + mid) <= i) lo = mid + 1; else hi = mid;
+                if (ld_off<IdxT>(p, mid) <= i) lo = mid + 1; else hi = mid;
             }
             const int64_t g = lo - 1;
-            covered = g >= 0 && g < p.NB && __ldg(p.offsets + g) >= 0 &&
-                      (int64_t)__ldg(p.offsets + g + 1) <= p.N;
+            covered = g >= 0 && g < p.NB && ld_off<IdxT>(p, g) >= 0 && ld_off<IdxT>(p, g + 1) <= p.N;
         }
         if (!covered) {
-            p.keys[i] = p.sentinel;
+            keys[i] = (KeyT)p.sentinel;
             p.vals[i] = 0u;
             if (p.bag_of != nullptr) p.bag_of[i] = -1;
         }
@@ -331,7 +349,7 @@ template <int LPR, int NV, int VB> constexpr int fwd_unroll(int rows) {
                : (32 / LPR >= rows ? 1 : rows / (32 / LPR));
 }
 
-template <typename WT, int VB, int LPR, int NV>
+template <typename WT, int VB, int LPR, int NV, typename IdxT>
 static void fwd_launch(Launch &L, const FwdParams &p) {
     // measured on bf16 D=128 tables: 4-row steps 3.12 ms vs 8-row 3.43 ms for
     // bags of ~20 lookups; 8-row steps 0.57 ms vs 4-row 0.70 ms for ~32
@@ -339,8 +357,10 @@ static void fwd_launch(Launch &L, const FwdParams &p) {
     constexpr int UL = fwd_unroll<LPR, NV, VB>(2 * TBE_FWD_ROWS);
     const bool long_bags = p.N >= (int64_t)TBE_FWD_LONG_BAG * p.NB;
     auto k = p.psw != nullptr
-                 ? (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, true> : tbe_fwd_kernel<WT, VB, LPR, NV, US, true>)
-                 : (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false> : tbe_fwd_kernel<WT, VB, LPR, NV, US, false>);
+                 ? (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, true, IdxT>
+                              : tbe_fwd_kernel<WT, VB, LPR, NV, US, true, IdxT>)
+                 : (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false, IdxT>
+                              : tbe_fwd_kernel<WT, VB, LPR, NV, US, false, IdxT>);
     const int grid = grid_for(L, k, 256, p.NB);
     L.before("tbe_fwd_gather");
     k<<<grid, 256, 0, L.stream>>>(p);
@@ -349,25 +369,35 @@ static void fwd_launch(Launch &L, const FwdParams &p) {
 
 // Rows are read as 16-byte lane vectors: a warp instruction covers 512 bytes
 // (fewer, larger requests measured faster than 8-byte vectors on this path).
-template <typename WT>
+template <typename WT, typename IdxT>
 static bool fwd_dispatch(Launch &L, const FwdParams &p, int row_bytes) {
     const RowPlan rp = row_plan(row_bytes / (int)sizeof(WT), (int)sizeof(WT));
     switch (rp.lpr * 10 + rp.nv) {
-    case 11: fwd_launch<WT, 16, 1, 1>(L, p); return true;
-    case 21: fwd_launch<WT, 16, 2, 1>(L, p); return true;
-    case 41: fwd_launch<WT, 16, 4, 1>(L, p); return true;
-    case 81: fwd_launch<WT, 16, 8, 1>(L, p); return true;
-    case 161: fwd_launch<WT, 16, 16, 1>(L, p); return true;
-    case 321: fwd_launch<WT, 16, 32, 1>(L, p); return true;
-    case 322: fwd_launch<WT, 16, 32, 2>(L, p); return true;
-    case 323: fwd_launch<WT, 16, 32, 3>(L, p); return true;
-    case 324: fwd_launch<WT, 16, 32, 4>(L, p); return true;
+    case 11: fwd_launch<WT, 16, 1, 1, IdxT>(L, p); return true;
+    case 21: fwd_launch<WT, 16, 2, 1, IdxT>(L, p); return true;
+    case 41: fwd_launch<WT, 16, 4, 1, IdxT>(L, p); return true;
+    case 81: fwd_launch<WT, 16, 8, 1, IdxT>(L, p); return true;
+    case 161: fwd_launch<WT, 16, 16, 1, IdxT>(L, p); return true;
+    case 321: fwd_launch<WT, 16, 32, 1, IdxT>(L, p); return true;
+    case 322: fwd_launch<WT, 16, 32, 2, IdxT>(L, p); return true;
+    case 323: fwd_launch<WT, 16, 32, 3, IdxT>(L, p); return true;
+    case 324: fwd_launch<WT, 16, 32, 4, IdxT>(L, p); return true;
     default: return false;
     }
 }
 
-static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *out, uint32_t *keys,
-                             uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status,
+template <typename IdxT>
+static bool fwd_dtype(Launch &L, const FwdParams &p, int dtype, int D) {
+    switch (dtype) {
+    case TBE_F32: return fwd_dispatch<float, IdxT>(L, p, D * 4);
+    case TBE_F16: return fwd_dispatch<__half, IdxT>(L, p, D * 2);
+    case TBE_BF16: return fwd_dispatch<__nv_bfloat16, IdxT>(L, p, D * 2);
+    default: return false;
+    }
+}
+
+static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *out, void *keys,
+                             uint32_t *vals, int32_t *bag_of, uint64_t sentinel, int32_t *status,
                              int32_t *counters) {
     FwdParams p;
     p.W = tab->weights;
@@ -393,44 +423,64 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
 }
 
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
-                          uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+                          uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
                           int32_t *status, int32_t *counters) {
     FwdParams p = make_params(tab, bt, out, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
-    bool ok = false;
     if (!row_plan(tab->D, tab->dtype == TBE_F32 ? 4 : 2).ok) return TBE_ERR_UNSUPPORTED_DIM;
-    switch (tab->dtype) {
-    case TBE_F32: ok = fwd_dispatch<float>(L, p, tab->D * 4); break;
-    case TBE_F16: ok = fwd_dispatch<__half>(L, p, tab->D * 2); break;
-    case TBE_BF16: ok = fwd_dispatch<__nv_bfloat16>(L, p, tab->D * 2); break;
-    default: return TBE_ERR_UNSUPPORTED_DTYPE;
-    }
+    if (tab->dtype != TBE_F32 && tab->dtype != TBE_F16 && tab->dtype != TBE_BF16)
+        return TBE_ERR_UNSUPPORTED_DTYPE;
+    const bool ok = bt->index_type == TBE_INDEX_I64 ? fwd_dtype<int64_t>(L, p, tab->dtype, tab->D)
+                                                    : fwd_dtype<int32_t>(L, p, tab->dtype, tab->D);
     return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
 }
 
-tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt, uint32_t *keys,
-                            uint32_t *vals, int32_t *bag_of, uint32_t sentinel, int32_t *status,
-                            int32_t *counters) {
+template <typename IdxT, typename KeyT> static void linearize_launch(Launch &L, const FwdParams &p) {
+    auto k = tbe_linearize_kernel<IdxT, KeyT>;
+    const int grid = grid_for(L, k, 256, p.NB);
+    L.before("tbe_linearize");
+    k<<<grid, 256, 0, L.stream>>>(p);
+    L.after();
+}
+
+tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt, void *keys,
+                            int key_bytes, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
+                            int32_t *status, int32_t *counters) {
     FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
-    const int grid = grid_for(L, tbe_linearize_kernel, 256, p.NB);
-    L.before("tbe_linearize");
-    tbe_linearize_kernel<<<grid, 256, 0, L.stream>>>(p);
-    L.after();
+    const bool i64 = bt->index_type == TBE_INDEX_I64;
+    if (key_bytes == 8) {
+        if (i64) linearize_launch<int64_t, uint64_t>(L, p);
+        else linearize_launch<int32_t, uint64_t>(L, p);
+    } else {
+        if (i64) linearize_launch<int64_t, uint32_t>(L, p);
+        else linearize_launch<int32_t, uint32_t>(L, p);
+    }
     return TBE_OK;
 }
 
-tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt, uint32_t *keys,
-                                uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+template <typename IdxT, typename KeyT> static void fixup_launch(Launch &L, const FwdParams &p) {
+    int64_t grid = (p.N + 255) / 256;
+    if (grid > (int64_t)L.num_sms * 4) grid = (int64_t)L.num_sms * 4;
+    L.before("tbe_offsets_fixup");
+    tbe_offsets_fixup_kernel<IdxT, KeyT><<<(unsigned)grid, 256, 0, L.stream>>>(p);
+    L.after();
+}
+
+tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt, void *keys,
+                                int key_bytes, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
                                 const int32_t *counters) {
     FwdParams p = make_params(tab, bt, nullptr, keys, vals, bag_of, sentinel, nullptr,
                               const_cast<int32_t *>(counters));
     if (p.N == 0) return TBE_OK;
-    int64_t grid = (p.N + 255) / 256;
-    if (grid > (int64_t)L.num_sms * 4) grid = (int64_t)L.num_sms * 4;
-    L.before("tbe_offsets_fixup");
-    tbe_offsets_fixup_kernel<<<(unsigned)grid, 256, 0, L.stream>>>(p);
-    L.after();
+    const bool i64 = bt->index_type == TBE_INDEX_I64;
+    if (key_bytes == 8) {
+        if (i64) fixup_launch<int64_t, uint64_t>(L, p);
+        else fixup_launch<int32_t, uint64_t>(L, p);
+    } else {
+        if (i64) fixup_launch<int64_t, uint32_t>(L, p);
+        else fixup_launch<int32_t, uint32_t>(L, p);
+    }
     return TBE_OK;
 }
 

@@ -132,8 +132,8 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int k) {
 struct HistFwdParams {
     const __half *W;
     const int64_t *table_offset;
-    const int32_t *indices;
-    const int32_t *offsets;
+    const void *indices;  // IdxT [N]
+    const void *offsets;  // IdxT [T*B+1]
     float *out;
     uint16_t *hist;       // nullable
     int32_t *status;
@@ -161,8 +161,11 @@ struct HistFwdSmem {
     uint32_t tmem_base;
 };
 
+template <typename IdxT>
 __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdParams p) {
     extern __shared__ unsigned char smem_raw[];
+    const IdxT *offsets = reinterpret_cast<const IdxT *>(p.offsets);
+    const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
     // 1024-byte alignment of the operand tiles (the swizzle pattern is anchored there)
     HistFwdSmem &S = *reinterpret_cast<HistFwdSmem *>(
         (void *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
     int oob = 0;
     // offsets[0] != 0 or offsets[T*B] != N leaves lookups outside every bag
     if (blockIdx.x == 0 && tid == 0 &&
-        (__ldg(p.offsets) != 0 || (int64_t)__ldg(p.offsets + p.T * p.B) != p.N)) {
+        ((int64_t)__ldg(offsets) != 0 || (int64_t)__ldg(offsets + p.T * p.B) != p.N)) {
         atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
         if (p.counters != nullptr) p.counters[C_MALFORMED] = 1;
     }
@@ -218,11 +221,11 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
         for (int i = tid; i < HT_BAGS * CNT_STRIDE; i += HF_THREADS) S.cnt[i] = 0;
         if (tid < HT_BAGS) {
             // a well-formed bag has 0 <= start <= end <= N; any other is empty
-            int32_t s0 = 0, s1 = 0;
+            int64_t s0 = 0, s1 = 0;
             if (tid < nb) {
-                s0 = __ldg(p.offsets + g0 + tid);
-                s1 = __ldg(p.offsets + g0 + tid + 1);
-                if (!(s0 <= s1 && s0 >= 0 && (int64_t)s1 <= p.N)) {
+                s0 = (int64_t)__ldg(offsets + g0 + tid);
+                s1 = (int64_t)__ldg(offsets + g0 + tid + 1);
+                if (!(s0 <= s1 && s0 >= 0 && s1 <= p.N)) {
                     atomicOr(p.status + 1, TBE_FLAG_BAD_OFFSETS);
                     if (p.counters != nullptr) {
                         p.counters[C_MALFORMED] = 1;
@@ -231,8 +234,8 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
                     s0 = s1 = 0;
                 }
             }
-            S.bs[tid] = s0;
-            S.be[tid] = s1;
+            S.bs[tid] = (int32_t)s0;
+            S.be[tid] = (int32_t)s1;
         }
         __syncthreads();
         // count the tile's lookups: a warp takes CB bags at a time and its
@@ -252,13 +255,13 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
                     maxlen = max(maxlen, be[j] - bs[j]);
                 }
                 for (int32_t k = 0; k < maxlen; k += 32 * CU) {
-                    int32_t v[CB][CU];
+                    IdxT v[CB][CU];
 #pragma unroll
                     for (int j = 0; j < CB; ++j)
 #pragma unroll
                         for (int u = 0; u < CU; ++u) {
                             const int32_t pos = bs[j] + k + u * 32 + lane;
-                            v[j][u] = pos < be[j] ? __ldg(p.indices + pos) : 0;
+                            v[j][u] = pos < be[j] ? __ldg(indices + pos) : IdxT(0);
                         }
 #pragma unroll
                     for (int j = 0; j < CB; ++j)
@@ -266,9 +269,10 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
                         for (int u = 0; u < CU; ++u) {
                             const int32_t pos = bs[j] + k + u * 32 + lane;
                             if (pos >= be[j]) continue;
-                            const int32_t idx = v[j][u];
+                            const IdxT idx = v[j][u];
                             if (idx >= 0 && (int64_t)idx < E)
-                                atomicAdd(&S.cnt[(r0 + j) * CNT_STRIDE + (idx >> 1)], 1u << ((idx & 1) * 16));
+                                atomicAdd(&S.cnt[(r0 + j) * CNT_STRIDE + (int)(idx >> 1)],
+                                          1u << ((int)(idx & 1) * 16));
                             else
                                 ++oob;
                         }
@@ -663,7 +667,8 @@ static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_ba
     p.tiles_total = p.tiles_per_table * tab->T;
     p.do_mma = do_mma;
     const size_t smem = fwd_smem();
-    cached_smem_attr(L.dev, (const void *)tbe_hist_fwd_kernel, smem);
+    auto kern = bt->index_type == TBE_INDEX_I64 ? tbe_hist_fwd_kernel<int64_t> : tbe_hist_fwd_kernel<int32_t>;
+    cached_smem_attr(L.dev, (const void *)kern, smem);
     // CTAs per SM: shared memory (227 KB usable, 1 KB reserved per CTA) and
     // TMEM (512 columns, 128 per CTA) both allow 4 (64 registers x 256 threads allow 4)
     int per_sm = (int)((227 * 1024) / (smem + 1024));
@@ -674,7 +679,7 @@ static tbe_status hist_fwd_launch(Launch &L, const tbe_tables *tab, const tbe_ba
     p.tiles_per_cta = (p.tiles_total + grid - 1) / grid;
     grid = (p.tiles_total + p.tiles_per_cta - 1) / p.tiles_per_cta;
     L.before(do_mma ? "tbe_hist_fwd_umma" : "tbe_hist_count");
-    tbe_hist_fwd_kernel<<<(unsigned)grid, HF_THREADS, smem, L.stream>>>(p);
+    kern<<<(unsigned)grid, HF_THREADS, smem, L.stream>>>(p);
     L.after();
     return TBE_OK;
 }

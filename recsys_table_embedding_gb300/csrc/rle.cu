@@ -56,21 +56,22 @@ __device__ __forceinline__ int block_excl_scan(int x, int *tot_smem, int &total)
     return wp + y - x;
 }
 
-__global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const uint32_t *__restrict__ k,
-                                                                int64_t N, uint32_t sentinel,
+template <typename KeyT>
+__global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const KeyT *__restrict__ k,
+                                                                int64_t N, KeyT sentinel,
                                                                 int32_t *tile_heads,
                                                                 int32_t *counters) {
     __shared__ int tot[RLE_THREADS / 32];
     const int64_t base = (int64_t)blockIdx.x * RLE_TILE + threadIdx.x * RLE_IPT;
     int heads = 0;
-    uint32_t prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : 0xffffffffu;
+    KeyT prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : ~KeyT(0);
 #pragma unroll
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
         if (pos < N) {
             // keys >= sentinel (out-of-range lookups and lookups outside every
             // well-formed bag; they sort last) start no run
-            const uint32_t cur = __ldg(k + pos);
+            const KeyT cur = __ldg(k + pos);
             const bool first = pos == 0 || cur != prev;
             if (first && cur < sentinel) ++heads;
             if (cur >= sentinel && (pos == 0 || prev < sentinel)) counters[C_N_VALID] = (int32_t)pos;
@@ -104,15 +105,16 @@ __global__ void __launch_bounds__(1024) rle_scan_kernel(int32_t *tile_heads, int
     if (threadIdx.x == 0) counters[C_NUM_UNIQUE] = carry;
 }
 
+template <typename KeyT>
 __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
-    const uint32_t *__restrict__ k, int64_t N, uint32_t sentinel,
-    const int32_t *__restrict__ tile_base, uint32_t *unique_keys, int32_t *seg_off,
+    const KeyT *__restrict__ k, int64_t N, KeyT sentinel,
+    const int32_t *__restrict__ tile_base, KeyT *unique_keys, int32_t *seg_off,
     const int32_t *counters) {
     __shared__ int tot[RLE_THREADS / 32];
     const int64_t base = (int64_t)blockIdx.x * RLE_TILE + threadIdx.x * RLE_IPT;
-    uint32_t kk[RLE_IPT];
+    KeyT kk[RLE_IPT];
     unsigned headmask = 0;
-    uint32_t prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : 0xffffffffu;
+    KeyT prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : ~KeyT(0);
 #pragma unroll
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
@@ -135,13 +137,14 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
 // Long runs (SL >= sl_threshold) get a slot l and ceil(SL/chunk) chunk slots.
 // The order of slots depends on atomic arrival; results do not (each chunk
 // covers a fixed position range and partials are summed in chunk order).
-// Each chunk slot then gets a descriptor -- its position range, key, table,
-// long run, the run's first slot and chunk count, and the batch window of
-// its first lookup's bag -- so the long-run kernel reads one 32-byte record
-// per chunk.  With ordering on, each chunk is also counted in its window.
+// Each chunk slot then gets a descriptor -- its position range, key (low and
+// high 32 bits), long run, the run's first slot and chunk count, and the
+// batch window of its first lookup's bag -- so the long-run kernel reads one
+// 32-byte record per chunk.  With ordering on, each chunk is also counted in its window.
 struct RouteParams {
     const int32_t *seg_off;
-    const uint32_t *unique_keys;
+    const void *unique_keys;   // uint32 or uint64 (key64)
+    int key64;
     const uint32_t *vals;
     const int32_t *bag_of;
     const int64_t *table_offset;
@@ -193,8 +196,9 @@ __global__ void __launch_bounds__(256) chunk_desc_kernel(const RouteParams p) {
         const int r = __ldg(p.long_run + l);
         const int cb = __ldg(p.long_chunk_base + l);
         const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
-        const uint32_t key = __ldg(p.unique_keys + r);
-        const int t = table_of_key(p.table_offset, p.T, key);
+        const uint64_t key = p.key64 ? __ldg(reinterpret_cast<const unsigned long long *>(p.unique_keys) + r)
+                                     : __ldg(reinterpret_cast<const uint32_t *>(p.unique_keys) + r);
+        const int t = table_of_key(p.table_offset, p.T, (int64_t)key);
         const int32_t s = rs + (c - cb) * p.chunk;
         int w = 0;
         if (p.wshift >= 0) {
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(256) chunk_desc_kernel(const RouteParams p) {
             atomicAdd(wc + w, 1);
         }
         int4 *d = reinterpret_cast<int4 *>(p.chunk_desc + (int64_t)c * 8);
-        d[0] = make_int4(s, min(s + p.chunk, re), (int)key, t);
+        d[0] = make_int4(s, min(s + p.chunk, re), (int)(uint32_t)key, (int)(uint32_t)(key >> 32));
         d[1] = make_int4(l, cb, (re - rs + p.chunk - 1) / p.chunk, w);
     }
     __syncthreads();
@@ -277,15 +281,25 @@ tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     const int wshift = order ? chunk_window_shift(a.B, a.T) : -1;
     const int nwin = order ? a.T * (int)((a.B + (int64_t(1) << wshift) - 1) >> wshift) : 0;
     L.before("tbe_rle_count");
-    rle_count_kernel<<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(a.sorted_keys, a.N, a.sentinel,
-                                                                     tile_heads, a.counters);
+    if (a.key_bytes == 8)
+        rle_count_kernel<uint64_t><<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
+            (const uint64_t *)a.sorted_keys, a.N, a.sentinel, tile_heads, a.counters);
+    else
+        rle_count_kernel<uint32_t><<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
+            (const uint32_t *)a.sorted_keys, a.N, (uint32_t)a.sentinel, tile_heads, a.counters);
     L.after();
     L.before("tbe_rle_scan");
     rle_scan_kernel<<<1, 1024, 0, L.stream>>>(tile_heads, ntiles, a.counters);
     L.after();
     L.before("tbe_rle_write");
-    rle_write_kernel<<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
-        a.sorted_keys, a.N, a.sentinel, tile_heads, a.unique_keys, a.seg_off, a.counters);
+    if (a.key_bytes == 8)
+        rle_write_kernel<uint64_t><<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
+            (const uint64_t *)a.sorted_keys, a.N, a.sentinel, tile_heads, (uint64_t *)a.unique_keys,
+            a.seg_off, a.counters);
+    else
+        rle_write_kernel<uint32_t><<<(unsigned)ntiles, RLE_THREADS, 0, L.stream>>>(
+            (const uint32_t *)a.sorted_keys, a.N, (uint32_t)a.sentinel, tile_heads,
+            (uint32_t *)a.unique_keys, a.seg_off, a.counters);
     L.after();
     if (order) {
         L.before("tbe_rle_zero");
@@ -295,6 +309,7 @@ tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     RouteParams p;
     p.seg_off = a.seg_off;
     p.unique_keys = a.unique_keys;
+    p.key64 = a.key_bytes == 8;
     p.vals = a.sorted_vals;
     p.bag_of = a.bag_of;
     p.table_offset = a.table_offset;

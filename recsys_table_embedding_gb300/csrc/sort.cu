@@ -1,8 +1,9 @@
 // Stable LSD radix sort of (key, payload) pairs: the sort step of the batch
 // inversion (FBTriton TBE redesign, accesspath.com, "transpose_embedding_input";
-// decision checklist item 6: int32 keys halve the sort-key width).  Only the
+// decision checklist item 6: int32 keys halve the sort-key width).  Keys are
+// 32-bit, or 64-bit when the linearised range reaches 2^31.  Only the
 // significant key bits are sorted, in ceil(key_bits / 9) passes of at most
-// 9 bits (512 buckets): 26-bit keys take 3 passes.
+// 9 bits (512 buckets): 26-bit keys take 3 passes, 32-bit keys 4.
 //
 // Design (onesweep: one read and one write of the pairs per pass, digit
 // prefixes across tiles by decoupled look-back):
@@ -34,7 +35,7 @@ constexpr int SORT_TILE = SORT_THREADS * SORT_IPT;   // 4096
 constexpr uint32_t ST_AGG = 1u << 30;
 constexpr uint32_t ST_INC = 2u << 30;
 constexpr uint32_t ST_MASK = (1u << 30) - 1;
-constexpr int MAX_PASSES = 4;
+constexpr int MAX_PASSES = 8;   // 64-bit keys: at most 7 passes of 9 bits
 #ifndef TBE_SORT_LOOKBACK
 #define TBE_SORT_LOOKBACK 8
 #endif
@@ -67,32 +68,52 @@ static SortWs carve(void *ws, int64_t N) {
 
 size_t sort_workspace_bytes(int64_t N, int key_bits) {
     const int64_t ntiles = (N + SORT_TILE - 1) / SORT_TILE;
-    (void)key_bits;
-    return MAX_PASSES * RADIX * 4 + 256 + (size_t)MAX_PASSES * ntiles * RADIX * 4 + 256;
+    int passes = num_passes(key_bits);
+    if (passes < 1) passes = 1;
+    return MAX_PASSES * RADIX * 4 + 256 + (size_t)passes * ntiles * RADIX * 4 + 256;
 }
 
-__global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t *__restrict__ keys, int64_t N,
+// 16-byte vector of keys
+template <typename KeyT> struct KeyVec;
+template <> struct KeyVec<uint32_t> {
+    static constexpr int K = 4;
+    static __device__ __forceinline__ void load(const uint32_t *p, int64_t i, uint32_t (&k)[4]) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+        k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+    }
+};
+template <> struct KeyVec<uint64_t> {
+    static constexpr int K = 2;
+    static __device__ __forceinline__ void load(const uint64_t *p, int64_t i, uint64_t (&k)[2]) {
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2 *>(p) + i);
+        k[0] = v.x; k[1] = v.y;
+    }
+};
+
+template <typename KeyT>
+__global__ void __launch_bounds__(256) radix_hist_kernel(const KeyT *__restrict__ keys, int64_t N,
                                                          int passes, int bits, uint32_t *hist,
                                                          uint32_t *zero, int64_t zero_words) {
+    constexpr int K = KeyVec<KeyT>::K;
     const uint32_t mask = (1u << bits) - 1;
     __shared__ uint32_t sh[MAX_PASSES * RADIX];
     for (int i = threadIdx.x; i < MAX_PASSES * RADIX; i += blockDim.x) sh[i] = 0;
     __syncthreads();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t N4 = N / 4;
-    for (int64_t i = tid; i < N4; i += stride) {
-        const uint4 k4 = __ldg(reinterpret_cast<const uint4 *>(keys) + i);
-        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+    const int64_t NV = N / K;
+    for (int64_t i = tid; i < NV; i += stride) {
+        KeyT kk[K];
+        KeyVec<KeyT>::load(keys, i, kk);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < K; ++e)
             for (int ps = 0; ps < passes; ++ps)
-                atomicAdd(&sh[ps * RADIX + ((kk[e] >> (ps * bits)) & mask)], 1u);
+                atomicAdd(&sh[ps * RADIX + (uint32_t)((kk[e] >> (ps * bits)) & mask)], 1u);
     }
-    for (int64_t i = N4 * 4 + tid; i < N; i += stride) {
-        const uint32_t k = __ldg(keys + i);
+    for (int64_t i = NV * K + tid; i < N; i += stride) {
+        const KeyT k = __ldg(keys + i);
         for (int ps = 0; ps < passes; ++ps)
-            atomicAdd(&sh[ps * RADIX + ((k >> (ps * bits)) & mask)], 1u);
+            atomicAdd(&sh[ps * RADIX + (uint32_t)((k >> (ps * bits)) & mask)], 1u);
     }
     for (int64_t i = tid; i < zero_words; i += stride) zero[i] = 0;
     __syncthreads();
@@ -122,8 +143,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-struct PassSmem {
-    uint32_t keys[SORT_TILE];
+template <typename KeyT> struct PassSmem {
+    KeyT keys[SORT_TILE];
     uint32_t vals[SORT_TILE];
     uint32_t warp_cnt[SORT_WARPS][RADIX];   // counts, then exclusive warp prefixes
     uint32_t count[RADIX];
@@ -133,13 +154,14 @@ struct PassSmem {
     uint32_t tile;
 };
 
+template <typename KeyT>
 __global__ void __launch_bounds__(SORT_THREADS, 2)
-radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
-                      uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t N,
+radix_onesweep_kernel(const KeyT *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
+                      KeyT *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t N,
                       int shift, uint32_t mask, const uint32_t *__restrict__ bucket, uint32_t *status,
                       uint32_t *ticket, int32_t *err) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    PassSmem &S = *reinterpret_cast<PassSmem *>(smem_raw);
+    PassSmem<KeyT> &S = *reinterpret_cast<PassSmem<KeyT> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) S.tile = atomicAdd(ticket, 1u);
@@ -150,19 +172,20 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
 
     // warp-striped load: item i of lane l in warp w sits at tile position
     // w*32*IPT + i*32 + l, so (i, lane) order within a warp is input order
-    uint32_t k[SORT_IPT], v[SORT_IPT], rank[SORT_IPT];
+    KeyT k[SORT_IPT];
+    uint32_t v[SORT_IPT], rank[SORT_IPT];
 #pragma unroll
     for (int i = 0; i < SORT_IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
         const bool ok = pos < N;
-        k[i] = ok ? __ldg(keys_in + pos) : 0xffffffffu;
+        k[i] = ok ? __ldg(keys_in + pos) : ~KeyT(0);
         v[i] = ok ? __ldg(vals_in + pos) : 0u;
     }
     const unsigned lt = lanemask_lt();
 #pragma unroll
     for (int i = 0; i < SORT_IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
-        const uint32_t d = pos < N ? ((k[i] >> shift) & mask) : RADIX;   // RADIX = padding
+        const uint32_t d = pos < N ? (uint32_t)((k[i] >> shift) & mask) : RADIX;   // RADIX = padding
         const unsigned peers = __match_any_sync(FULL, d);
         const int leader = __ffs(peers) - 1;
         uint32_t base = 0;
@@ -254,7 +277,7 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     for (int i = 0; i < SORT_IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
         if (pos < N) {
-            const uint32_t d = (k[i] >> shift) & mask;
+            const uint32_t d = (uint32_t)((k[i] >> shift) & mask);
             const uint32_t lp = S.local_off[d] + S.warp_cnt[warp][d] + rank[i];
             S.keys[lp] = k[i];
             S.vals[lp] = v[i];
@@ -265,8 +288,8 @@ radix_onesweep_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__re
     const int64_t rem = N - tile_base;
     const int n = rem < SORT_TILE ? (int)rem : SORT_TILE;
     for (int j = tid; j < n; j += SORT_THREADS) {
-        const uint32_t key = S.keys[j];
-        const uint32_t d = (key >> shift) & mask;
+        const KeyT key = S.keys[j];
+        const uint32_t d = (uint32_t)((key >> shift) & mask);
         const uint32_t gp = S.global_base[d] + (j - S.local_off[d]);
         if ((int64_t)gp < N) {   // always true unless a look-back gave up (flagged)
             keys_out[gp] = key;
@@ -281,8 +304,50 @@ __global__ void fill_u32_kernel(uint32_t *p, int64_t n, uint32_t v) {
         p[i] = v;
 }
 
-tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *keys_b,
-                       uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
+template <typename KeyT>
+static void sort_passes(Launch &L, KeyT *keys_a, uint32_t *vals_a, KeyT *keys_b, uint32_t *vals_b,
+                        int64_t N, int passes, int bits, const SortWs &s, int32_t *status) {
+    const int64_t zero_words = (int64_t)passes * s.ntiles * RADIX;
+    L.before("tbe_sort_zero");
+    fill_u32_kernel<<<1, 256, 0, L.stream>>>(s.hist, MAX_PASSES * RADIX + 64, 0u);
+    L.after();
+
+    const int64_t nvec = N / KeyVec<KeyT>::K;
+    int hist_grid = (int)((nvec + 255) / 256);
+    if (hist_grid > L.num_sms * 4) hist_grid = L.num_sms * 4;
+    if (hist_grid < 1) hist_grid = 1;
+    L.before("tbe_sort_histogram");
+    radix_hist_kernel<KeyT><<<hist_grid, 256, 0, L.stream>>>(keys_a, N, passes, bits, s.hist, s.status,
+                                                             zero_words);
+    L.after();
+    L.before("tbe_sort_buckets");
+    radix_bucket_kernel<<<passes, RADIX, 0, L.stream>>>(s.hist);
+    L.after();
+
+    const size_t smem = sizeof(PassSmem<KeyT>);
+    static_assert(sizeof(PassSmem<uint64_t>) * 2 < 227 * 1024, "pass shared memory");
+    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel<KeyT>, smem);
+    const KeyT *ki = keys_a;
+    const uint32_t *vi = vals_a;
+    KeyT *ko = keys_b;
+    uint32_t *vo = vals_b;
+    for (int ps = 0; ps < passes; ++ps) {
+        L.before("tbe_sort_onesweep");
+        radix_onesweep_kernel<KeyT><<<(unsigned)s.ntiles, SORT_THREADS, smem, L.stream>>>(
+            ki, vi, ko, vo, N, ps * bits, (1u << bits) - 1, s.hist + ps * RADIX,
+            s.status + (int64_t)ps * s.ntiles * RADIX, s.tickets + ps, status + 1);
+        L.after();
+        const KeyT *tk = ko;
+        const uint32_t *tv = vo;
+        ko = const_cast<KeyT *>(ki);
+        vo = const_cast<uint32_t *>(vi);
+        ki = tk;
+        vi = tv;
+    }
+}
+
+tbe_status launch_sort(Launch &L, void *keys_a, uint32_t *vals_a, void *keys_b, uint32_t *vals_b,
+                       int64_t N, int key_bits, int key_bytes, void *ws, int32_t *status,
                        bool *in_b) {
     const int passes = num_passes(key_bits);
     const int bits = digit_bits(key_bits);
@@ -292,41 +357,13 @@ tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *
         return TBE_OK;
     }
     if (passes > MAX_PASSES) return TBE_ERR_KEY_RANGE;
-    SortWs s = carve(ws, N);
-    const int64_t zero_words = (int64_t)passes * s.ntiles * RADIX;
-
-    L.before("tbe_sort_zero");
-    fill_u32_kernel<<<1, 256, 0, L.stream>>>(s.hist, MAX_PASSES * RADIX + 64, 0u);
-    L.after();
-
-    int hist_grid = (int)((N / 4 + 255) / 256);
-    if (hist_grid > L.num_sms * 4) hist_grid = L.num_sms * 4;
-    if (hist_grid < 1) hist_grid = 1;
-    L.before("tbe_sort_histogram");
-    radix_hist_kernel<<<hist_grid, 256, 0, L.stream>>>(keys_a, N, passes, bits, s.hist, s.status,
-                                                       zero_words);
-    L.after();
-    L.before("tbe_sort_buckets");
-    radix_bucket_kernel<<<passes, RADIX, 0, L.stream>>>(s.hist);
-    L.after();
-
-    const size_t smem = sizeof(PassSmem);
-    static_assert(sizeof(PassSmem) < 227 * 1024, "pass shared memory");
-    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel, smem);
-    const uint32_t *ki = keys_a, *vi = vals_a;
-    uint32_t *ko = keys_b, *vo = vals_b;
-    for (int ps = 0; ps < passes; ++ps) {
-        L.before("tbe_sort_onesweep");
-        radix_onesweep_kernel<<<(unsigned)s.ntiles, SORT_THREADS, smem, L.stream>>>(
-            ki, vi, ko, vo, N, ps * bits, (1u << bits) - 1, s.hist + ps * RADIX,
-            s.status + (int64_t)ps * s.ntiles * RADIX, s.tickets + ps, status + 1);
-        L.after();
-        const uint32_t *tk = ko, *tv = vo;
-        ko = const_cast<uint32_t *>(ki);
-        vo = const_cast<uint32_t *>(vi);
-        ki = tk;
-        vi = tv;
-    }
+    const SortWs s = carve(ws, N);
+    if (key_bytes == 8)
+        sort_passes<uint64_t>(L, (uint64_t *)keys_a, vals_a, (uint64_t *)keys_b, vals_b, N, passes, bits,
+                              s, status);
+    else
+        sort_passes<uint32_t>(L, (uint32_t *)keys_a, vals_a, (uint32_t *)keys_b, vals_b, N, passes, bits,
+                              s, status);
     return TBE_OK;
 }
 
@@ -362,12 +399,12 @@ tbe_status launch_sort_selftest(Launch &L, void *ws, int32_t *status) {
     L.before("tbe_selftest_init");
     sort_selftest_init_kernel<<<8, 256, 0, L.stream>>>(w, words, ticket);
     L.after();
-    const size_t smem = sizeof(PassSmem);
-    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel, smem);
+    const size_t smem = sizeof(PassSmem<uint32_t>);
+    cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel<uint32_t>, smem);
     L.before("tbe_sort_onesweep");
-    radix_onesweep_kernel<<<1, SORT_THREADS, smem, L.stream>>>(keys_in, vals_in, keys_out, vals_out,
-                                                                SELFTEST_N, 0, RADIX - 1, bucket,
-                                                                look, ticket, status + 1);
+    radix_onesweep_kernel<uint32_t><<<1, SORT_THREADS, smem, L.stream>>>(
+        keys_in, vals_in, keys_out, vals_out, SELFTEST_N, 0, RADIX - 1, bucket, look, ticket,
+        status + 1);
     L.after();
     return TBE_OK;
 }

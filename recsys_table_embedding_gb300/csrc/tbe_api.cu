@@ -100,7 +100,7 @@ static int bits_for(int64_t v) {   // bits needed to represent v >= 0
 struct Problem {
     int64_t N, B, NB, rows_total, max_rows;
     int T, D, dtype;
-    int key_bits;
+    int key_bits, key_bytes, index_type;
     int path;           // 1 generic, 2 histogram
     int payload_pos;
     int64_t max_long, max_chunks;
@@ -130,8 +130,11 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     if ((int64_t)tab->T * bt->B >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
     if (bt->offsets == nullptr) return TBE_ERR_NULL_POINTER;
     if (bt->N > 0 && bt->indices == nullptr) return TBE_ERR_NULL_POINTER;
-    if (!aligned(tab->weights, 16) || !aligned(tab->table_offset, 8) || !aligned(bt->offsets, 4) ||
-        !aligned(bt->indices, 4) || !aligned(bt->per_sample_weights, 4))
+    if (bt->index_type != TBE_INDEX_I32 && bt->index_type != TBE_INDEX_I64)
+        return TBE_ERR_INVALID_ARGUMENT;
+    const size_t isz = bt->index_type == TBE_INDEX_I64 ? 8 : 4;
+    if (!aligned(tab->weights, 16) || !aligned(tab->table_offset, 8) || !aligned(bt->offsets, isz) ||
+        !aligned(bt->indices, isz) || !aligned(bt->per_sample_weights, 4))
         return TBE_ERR_MISALIGNED;
     const int64_t *to = tab->table_offset_host;
     if (to[0] != 0) return TBE_ERR_INVALID_ARGUMENT;
@@ -141,9 +144,10 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
         if (to[t + 1] - to[t] > max_rows) max_rows = to[t + 1] - to[t];
     }
     const int64_t rows_total = to[tab->T];
-    // int32 linearised keys (decision checklist item 6); rows_total itself
-    // is the sentinel key of out-of-range lookups, so it must fit too
-    if (rows_total >= (int64_t(1) << 31) - 1) return TBE_ERR_KEY_RANGE;
+    // linearised keys: int32 while the range (rows_total itself is the
+    // sentinel key of ignored lookups) stays below 2^31 - 1 (decision
+    // checklist item 6), 64-bit beyond
+    if (rows_total >= (int64_t(1) << 62)) return TBE_ERR_KEY_RANGE;
     tbe_config c = defaults(cfg);
     if (c.long_run_mode < 0 || c.long_run_mode > 2 || c.hist_mode < 0 || c.hist_mode > 2)
         return TBE_ERR_INVALID_ARGUMENT;
@@ -158,6 +162,11 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     pr->rows_total = rows_total;
     pr->max_rows = max_rows;
     pr->key_bits = bits_for(rows_total);
+    pr->key_bytes = rows_total < (int64_t(1) << 31) - 1 ? 4 : 8;
+    if (c.key_bytes != 0 && c.key_bytes != 4 && c.key_bytes != 8) return TBE_ERR_INVALID_ARGUMENT;
+    if (c.key_bytes == 4 && pr->key_bytes == 8) return TBE_ERR_KEY_RANGE;
+    if (c.key_bytes == 8) pr->key_bytes = 8;
+    pr->index_type = bt->index_type;
     pr->payload_pos = bt->per_sample_weights != nullptr ? 1 : 0;
     pr->sl_threshold = c.sl_threshold;
     pr->chunk = c.chunk;
@@ -199,13 +208,14 @@ static MetaLayout meta_layout(const Problem &pr) {
         return at;
     };
     const size_t N = (size_t)pr.N;
+    const size_t kb = (size_t)pr.key_bytes;
     if (pr.path == 1) {
-        m.keys_a = take(N * 4 + 16);
+        m.keys_a = take(N * kb + 16);
         m.vals_a = take(N * 4 + 16);
-        m.keys_b = take(N * 4 + 16);
+        m.keys_b = take(N * kb + 16);
         m.vals_b = take(N * 4 + 16);
         m.bag_of = pr.payload_pos ? take(N * 4 + 16) : (size_t)-1;
-        m.unique_keys = take(N * 4 + 16);
+        m.unique_keys = take(N * kb + 16);
         m.seg_off = take((N + 1) * 4 + 16);
         m.counters = take(C_COUNT * 4);
         m.long_run = take((size_t)pr.max_long * 4);
@@ -241,7 +251,8 @@ static size_t workspace_size(const tbe_tables *tab, const tbe_batch *bt, const P
 static tbe_status check_meta(const tbe_meta *meta, const Problem &pr) {
     if (meta->bound_N != pr.N || meta->bound_B != pr.B || meta->bound_T != pr.T ||
         meta->path != pr.path || meta->payload_is_pos != pr.payload_pos ||
-        meta->rows_total != pr.rows_total)
+        meta->rows_total != pr.rows_total || meta->key_bytes != pr.key_bytes ||
+        meta->index_type != pr.index_type)
         return TBE_ERR_META;
     return TBE_OK;
 }
@@ -255,12 +266,12 @@ static tbe_status finish(const Launch &L, tbe_status st) {
 // malformed-offsets fixup, sort, RLE/route (generic path)
 static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
                                 tbe_meta *meta, const Problem &pr, void *ws, int32_t *status) {
-    tbe_status st = launch_offsets_fixup(L, tab, bt, meta->keys_a, meta->vals_a, meta->bag_of,
-                                         (uint32_t)pr.rows_total, meta->counters);
+    tbe_status st = launch_offsets_fixup(L, tab, bt, meta->keys_a, pr.key_bytes, meta->vals_a,
+                                         meta->bag_of, (uint64_t)pr.rows_total, meta->counters);
     if (st != TBE_OK) return st;
     bool in_b = false;
     st = launch_sort(L, meta->keys_a, meta->vals_a, meta->keys_b, meta->vals_b, pr.N, pr.key_bits,
-                     ws, status, &in_b);
+                     pr.key_bytes, ws, status, &in_b);
     if (st != TBE_OK) return st;
     meta->sorted_keys = in_b ? meta->keys_b : meta->keys_a;
     meta->sorted_vals = in_b ? meta->vals_b : meta->vals_a;
@@ -270,7 +281,8 @@ static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batc
     a.bag_of = meta->bag_of;
     a.N = pr.N;
     a.B = pr.B;
-    a.sentinel = (uint32_t)pr.rows_total;
+    a.sentinel = (uint64_t)pr.rows_total;
+    a.key_bytes = pr.key_bytes;
     a.payload_pos = meta->payload_is_pos;
     a.unique_keys = meta->unique_keys;
     a.seg_off = meta->seg_off;
@@ -347,14 +359,16 @@ tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes, const t
     meta->payload_is_pos = pr.payload_pos;
     meta->key_bits = pr.key_bits;
     meta->rows_total = pr.rows_total;
-    meta->keys_a = (uint32_t *)at(L.keys_a);
+    meta->key_bytes = pr.key_bytes;
+    meta->index_type = pr.index_type;
+    meta->keys_a = at(L.keys_a);
     meta->vals_a = (uint32_t *)at(L.vals_a);
-    meta->keys_b = (uint32_t *)at(L.keys_b);
+    meta->keys_b = at(L.keys_b);
     meta->vals_b = (uint32_t *)at(L.vals_b);
     meta->sorted_keys = meta->keys_a;
     meta->sorted_vals = meta->vals_a;
     meta->bag_of = (int32_t *)at(L.bag_of);
-    meta->unique_keys = (uint32_t *)at(L.unique_keys);
+    meta->unique_keys = at(L.unique_keys);
     meta->seg_off = (int32_t *)at(L.seg_off);
     meta->counters = (int32_t *)at(L.counters);
     meta->long_run = (int32_t *)at(L.long_run);
@@ -387,9 +401,15 @@ tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *
                                  meta ? meta->counters : nullptr);
         return finish(L, st);
     }
-    st = launch_forward(L, tables, batch, out, meta ? meta->keys_a : nullptr,
-                        meta ? meta->vals_a : nullptr, meta ? meta->bag_of : nullptr,
-                        (uint32_t)pr.rows_total, dev_status, meta ? meta->counters : nullptr);
+    // the forward kernel writes 32-bit keys itself; 64-bit keys come from
+    // the linearize kernel after it
+    const bool fused_keys = meta != nullptr && pr.key_bytes == 4;
+    st = launch_forward(L, tables, batch, out, fused_keys ? (uint32_t *)meta->keys_a : nullptr,
+                        fused_keys ? meta->vals_a : nullptr, fused_keys ? meta->bag_of : nullptr,
+                        (uint64_t)pr.rows_total, dev_status, meta ? meta->counters : nullptr);
+    if (st == TBE_OK && meta != nullptr && !fused_keys)
+        st = launch_linearize(L, tables, batch, meta->keys_a, pr.key_bytes, meta->vals_a,
+                              meta->bag_of, (uint64_t)pr.rows_total, dev_status, meta->counters);
     if (st == TBE_OK && meta != nullptr)
         st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
     return finish(L, st);
@@ -408,8 +428,8 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
     launch_zero_counters(L, meta->counters);
     if (pr.path == 2)
         return finish(L, launch_hist_count(L, tables, batch, meta->hist, dev_status, meta->counters));
-    st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
-                          (uint32_t)pr.rows_total, dev_status, meta->counters);
+    st = launch_linearize(L, tables, batch, meta->keys_a, pr.key_bytes, meta->vals_a, meta->bag_of,
+                          (uint64_t)pr.rows_total, dev_status, meta->counters);
     if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, workspace, dev_status);
     return finish(L, st);
 }
@@ -462,7 +482,7 @@ const char *tbe_status_string(tbe_status s) {
     case TBE_ERR_UNSUPPORTED_DIM: return "unsupported embedding dimension";
     case TBE_ERR_UNSUPPORTED_DTYPE: return "unsupported weight dtype";
     case TBE_ERR_MISALIGNED: return "misaligned pointer";
-    case TBE_ERR_KEY_RANGE: return "linearised key range does not fit int32";
+    case TBE_ERR_KEY_RANGE: return "linearised key range of 2^62 rows or more";
     case TBE_ERR_BUFFER_TOO_SMALL: return "workspace or meta buffer too small";
     case TBE_ERR_META: return "meta not bound for this problem";
     case TBE_ERR_HISTOGRAM_SHAPE: return "histogram path does not cover this shape";
@@ -558,8 +578,8 @@ extern "C" tbe_status tbe_preprocess_static(const tbe_tables *tables, const tbe_
     // The sort zeroes its digit counts, tile tickets and look-back words, and
     // the RLE writes its tile counts before reading them, so the contents a
     // previous call left in the array are never read.
-    st = launch_linearize(L, tables, batch, meta->keys_a, meta->vals_a, meta->bag_of,
-                          (uint32_t)pr.rows_total, dev_status, meta->counters);
+    st = launch_linearize(L, tables, batch, meta->keys_a, pr.key_bytes, meta->vals_a, meta->bag_of,
+                          (uint64_t)pr.rows_total, dev_status, meta->counters);
     if (st == TBE_OK) st = run_inversion(L, tables, batch, meta, pr, scratch, dev_status);
     return finish(L, st);
 }

@@ -148,29 +148,31 @@ struct RowPlan {
 RowPlan row_plan(int D, int bytes_per_elem);
 
 // --- forward.cu
-// `counters` (nullable) receives C_MALFORMED / C_DECREASING.
+// `counters` (nullable) receives C_MALFORMED / C_DECREASING.  `keys`
+// (nullable) are 32-bit: 64-bit keys come from launch_linearize.
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
-                          uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+                          uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
                           int32_t *status, int32_t *counters);
-tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
-                            uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint32_t sentinel,
+tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt, void *keys,
+                            int key_bytes, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
                             int32_t *status, int32_t *counters);
 // After the forward or linearize kernel: when counters[C_MALFORMED] is set,
 // every lookup outside a well-formed bag gets the sentinel key (all lookups
 // when counters[C_DECREASING] is set), so that only lookups of well-formed
 // bags reach the backward.  Does nothing on well-formed batches.
-tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt,
-                                uint32_t *keys, uint32_t *vals, int32_t *bag_of,
-                                uint32_t sentinel, const int32_t *counters);
+tbe_status launch_offsets_fixup(Launch &L, const tbe_tables *tab, const tbe_batch *bt, void *keys,
+                                int key_bytes, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
+                                const int32_t *counters);
 // zero meta->counters (all C_COUNT words)
 void launch_zero_counters(Launch &L, int32_t *counters);
 
 // --- sort.cu: stable LSD radix sort of (key, val) pairs over the low
-// `key_bits` bits; result lands in (keys_a, vals_a) when the number of
-// passes is even, else in (keys_b, vals_b); returns which via *in_b.
+// `key_bits` bits (keys of key_bytes = 4 or 8); result lands in (keys_a,
+// vals_a) when the number of passes is even, else in (keys_b, vals_b);
+// returns which via *in_b.
 size_t sort_workspace_bytes(int64_t N, int key_bits);
-tbe_status launch_sort(Launch &L, uint32_t *keys_a, uint32_t *vals_a, uint32_t *keys_b,
-                       uint32_t *vals_b, int64_t N, int key_bits, void *ws, int32_t *status,
+tbe_status launch_sort(Launch &L, void *keys_a, uint32_t *vals_a, void *keys_b, uint32_t *vals_b,
+                       int64_t N, int key_bits, int key_bytes, void *ws, int32_t *status,
                        bool *in_b);
 
 // Self-test of the look-back's time limit (scratch of sort_selftest_bytes()).
@@ -192,13 +194,14 @@ bool chunk_order_on(int64_t B, int T);
 int chunk_window_shift(int64_t B, int T);
 
 struct RleArgs {
-    const uint32_t *sorted_keys;
+    const void *sorted_keys;
     const uint32_t *sorted_vals;
     const int32_t *bag_of;
     int64_t N, B;
-    uint32_t sentinel;
+    uint64_t sentinel;
+    int key_bytes;
     int payload_pos;
-    uint32_t *unique_keys;
+    void *unique_keys;
     int32_t *seg_off;
     int32_t *counters;
     int32_t *long_run;

@@ -23,6 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtbe_gb300.so")
 
 F32, F16, BF16 = 0, 1, 2
+INDEX_I32, INDEX_I64 = 0, 1
 LONG_AUTO, LONG_TWO_KERNEL, LONG_FUSED = 0, 1, 2
 HIST_AUTO, HIST_OFF, HIST_FORCE = 0, 1, 2
 STATUS_WORDS = 4
@@ -51,7 +52,7 @@ i32, i64 = ctypes.c_int32, ctypes.c_int64
 class tbe_config(ctypes.Structure):
     _fields_ = [("sl_threshold", i32), ("chunk", i32), ("long_run_mode", i32), ("hist_mode", i32),
                 ("kernel_events", P), ("kernel_names", P), ("n_kernel_events", i32),
-                ("kernel_events_used", P)]
+                ("kernel_events_used", P), ("key_bytes", i32)]
 
 
 class tbe_tables(ctypes.Structure):
@@ -61,12 +62,13 @@ class tbe_tables(ctypes.Structure):
 
 class tbe_batch(ctypes.Structure):
     _fields_ = [("indices", P), ("offsets", P), ("N", i64), ("B", i64),
-                ("per_sample_weights", P), ("weighted_tables", P)]
+                ("per_sample_weights", P), ("weighted_tables", P), ("index_type", i32)]
 
 
 class tbe_meta(ctypes.Structure):
     _fields_ = [("bound_N", i64), ("bound_B", i64), ("bound_T", i32), ("path", i32),
                 ("payload_is_pos", i32), ("key_bits", i32), ("rows_total", i64),
+                ("key_bytes", i32), ("index_type", i32),
                 ("sorted_keys", P), ("sorted_vals", P), ("keys_a", P), ("vals_a", P),
                 ("keys_b", P), ("vals_b", P), ("bag_of", P), ("unique_keys", P), ("seg_off", P),
                 ("counters", P), ("long_run", P), ("long_chunk_base", P), ("chunk_order", P),
@@ -133,10 +135,11 @@ def _stream(stream) -> int:
 
 
 def config(sl_threshold: int = 256, chunk: int = 256, long_run_mode: int = LONG_AUTO,
-           hist_mode: int = HIST_AUTO) -> tbe_config:
+           hist_mode: int = HIST_AUTO, key_bytes: int = 0) -> tbe_config:
     c = tbe_config()
     lib().tbe_config_default(ctypes.byref(c))
     c.sl_threshold, c.chunk, c.long_run_mode, c.hist_mode = sl_threshold, chunk, long_run_mode, hist_mode
+    c.key_bytes = key_bytes
     return c
 
 
@@ -159,17 +162,19 @@ class Tables:
 
 
 class Batch:
-    """One KeyedJagged CSR batch on the device."""
+    """One KeyedJagged CSR batch on the device: indices and offsets both int32
+    or both int64."""
 
     def __init__(self, indices: torch.Tensor, offsets: torch.Tensor, B: int,
                  per_sample_weights: Optional[torch.Tensor] = None,
                  weighted_tables: Optional[torch.Tensor] = None):
-        assert indices.dtype == torch.int32 and offsets.dtype == torch.int32
+        assert indices.dtype == offsets.dtype and indices.dtype in (torch.int32, torch.int64)
         self.indices, self.offsets, self.B = indices, offsets, int(B)
         self.per_sample_weights, self.weighted_tables = per_sample_weights, weighted_tables
         self.N = int(indices.numel())
+        itype = INDEX_I64 if indices.dtype == torch.int64 else INDEX_I32
         self.c = tbe_batch(_ptr(indices), _ptr(offsets), self.N, self.B, _ptr(per_sample_weights),
-                           _ptr(weighted_tables))
+                           _ptr(weighted_tables), itype)
 
 
 def tbe_query_sizes(tables: Tables, batch: Batch, cfg: Optional[tbe_config] = None):

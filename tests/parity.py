@@ -221,12 +221,21 @@ def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
         m = tbe.meta
         U, nv, nlong, nchunks = tbe.counters()
         res.update(num_unique=U, n_valid=nv, num_long=nlong, num_chunks=nchunks)
-        res["sorted_keys"] = meta_view(m, "sorted_keys", wl.N, torch.int32).cpu().numpy().view(np.uint32)
+        res["sorted_keys"] = meta_keys(m, "sorted_keys", wl.N)
         res["sorted_vals"] = meta_view(m, "sorted_vals", wl.N, torch.int32).cpu().numpy().view(np.uint32)
-        res["unique_keys"] = meta_view(m, "unique_keys", U, torch.int32).cpu().numpy().view(np.uint32)
+        res["unique_keys"] = meta_keys(m, "unique_keys", U)
+        res["key_bytes"] = m.c.key_bytes
         res["seg_off"] = meta_view(m, "seg_off", U + 1, torch.int32).cpu().numpy()
         res["payload_is_pos"] = m.c.payload_is_pos
     return res
+
+
+def meta_keys(meta, name: str, n: int) -> np.ndarray:
+    """n keys of a meta key array (4 or 8 bytes per key) as int64."""
+    from recsys_table_embedding_gb300 import meta_view
+    if meta.c.key_bytes == 8:
+        return meta_view(meta, name, n, torch.int64).cpu().numpy()
+    return meta_view(meta, name, n, torch.int32).cpu().numpy().view(np.uint32).astype(np.int64)
 
 
 def bag_of_position(wl, pos: np.ndarray) -> np.ndarray:
@@ -241,7 +250,7 @@ def check_inversion(wl, res, pre):
     nv = pre["n_valid"]
     assert res["n_valid"] == nv
     assert res["num_unique"] == pre["num_unique"]
-    np.testing.assert_array_equal(res["sorted_keys"][:nv].astype(np.int64), pre["sorted_keys"])
+    np.testing.assert_array_equal(res["sorted_keys"][:nv], pre["sorted_keys"])
     assert np.all(res["sorted_keys"][nv:] == wl.rows_total), "out-of-range lookups not last"
     if res["payload_is_pos"]:
         np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64), pre["sorted_pos"])

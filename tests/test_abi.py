@@ -39,13 +39,14 @@ FAKE = 0x7f0000000000   # 256-byte aligned fake device address, never dereferenc
 class Fake:
     """tables/batch structs with fake device pointers for host-only calls."""
 
-    def __init__(self, T=2, E=1000, D=64, dtype=0, B=16, N=128, psw=False, rows=None):
+    def __init__(self, T=2, E=1000, D=64, dtype=0, B=16, N=128, psw=False, rows=None, itype=0):
         from recsys_table_embedding_gb300 import tbe
         rows = rows if rows is not None else [E] * T
         self.to = np.zeros(len(rows) + 1, np.int64)
         self.to[1:] = np.cumsum(rows)
         self.tab = tbe.tbe_tables(FAKE, FAKE + 4096, self.to.ctypes.data, len(rows), D, dtype)
-        self.bt = tbe.tbe_batch(FAKE + 8192, FAKE + 16384, N, B, FAKE + 32768 if psw else None, None)
+        self.bt = tbe.tbe_batch(FAKE + 8192, FAKE + 16384, N, B, FAKE + 32768 if psw else None, None,
+                                itype)
         self.tbe = tbe
 
     def sizes(self, cfg=None):
@@ -87,7 +88,8 @@ def test_query_sizes_and_meta_bind_layout():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(D=6), 3), (dict(D=4, dtype=1), 3), (dict(D=1024, dtype=0), 3), (dict(dtype=7), 4),
-    (dict(N=1 << 30), 2), (dict(rows=[2**30, 2**30]), 6), (dict(rows=[5, -1]), 2),
+    (dict(N=1 << 30), 2), (dict(rows=[2**30, 2**30]), 0), (dict(rows=[2**61, 2**61]), 6),
+    (dict(rows=[5, -1]), 2), (dict(itype=2), 2), (dict(itype=1), 0),
     # grad_out [B, T*D] float32 of 64 GB or more: gradient offsets would not fit 32 bits
     (dict(T=2, B=2**27, D=128), 2), (dict(T=2, B=2**25, D=128), 0),
 ])
@@ -136,3 +138,41 @@ def test_status_strings():
     L = lib()
     assert L.tbe_status_string(0) == b"ok"
     assert L.tbe_status_string(7).startswith(b"workspace")
+
+
+def test_key_width_follows_the_row_range():
+    # decision checklist item 6: int32 keys while the linearised range (with
+    # its sentinel) fits, 64-bit keys beyond; the key arrays grow to match
+    from recsys_table_embedding_gb300 import tbe
+    L = tbe.lib()
+
+    def bind(rows, cfg=None, itype=0):
+        f = Fake(rows=rows, N=10000, B=100, itype=itype)
+        st, mb, _ = f.sizes(cfg)
+        assert st == 0
+        m = tbe.tbe_meta()
+        assert L.tbe_meta_bind(ctypes.byref(m), FAKE, mb, ctypes.byref(f.tab), ctypes.byref(f.bt),
+                               ctypes.byref(cfg) if cfg else None) == 0
+        return m, mb
+
+    m4, mb4 = bind([2**30, 2**30 - 2])               # rows_total = 2^31 - 2: sentinel fits int32
+    assert m4.key_bytes == 4 and m4.key_bits == 31
+    m8, mb8 = bind([2**30, 2**30 - 1])               # rows_total = 2^31 - 1
+    assert m8.key_bytes == 8 and m8.key_bits == 31
+    assert mb8 >= mb4 + 3 * 4 * 10000 - 3 * 256      # three key arrays twice as wide (256-B aligned)
+    mf, _ = bind([100, 100], cfg=tbe.config(key_bytes=8))
+    assert mf.key_bytes == 8
+    m64, _ = bind([100, 100], itype=1)
+    assert m64.index_type == 1 and m64.key_bytes == 4
+    f = Fake(rows=[2**31])
+    assert f.sizes(tbe.config(key_bytes=4))[0] == 6  # 32-bit keys cannot hold this range
+    assert f.sizes(tbe.config(key_bytes=5))[0] == 2
+
+
+def test_int64_index_arrays_must_be_8_byte_aligned():
+    f = Fake(itype=1)
+    f.bt.indices = FAKE + 8196
+    assert f.sizes()[0] == 5
+    f = Fake(itype=0)
+    f.bt.indices = FAKE + 8196
+    assert f.sizes()[0] == 0

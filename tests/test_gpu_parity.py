@@ -253,8 +253,9 @@ def test_chunk_descriptors_and_window_order(B):
     assert np.all(re - rs >= 256)
     assert np.all((desc[:, 0] - rs) % 256 == 0)
     np.testing.assert_array_equal(desc[:, 1], np.minimum(desc[:, 0] + 256, re))
-    np.testing.assert_array_equal(desc[:, 2], keys[runs])
-    np.testing.assert_array_equal(desc[:, 3], np.searchsorted(wl.table_offset, keys[runs], side="right") - 1)
+    np.testing.assert_array_equal(desc[:, 2].astype(np.uint32) | (desc[:, 3].astype(np.int64) << 32),
+                                  keys[runs])
+    table = np.searchsorted(wl.table_offset, keys[runs], side="right") - 1
     np.testing.assert_array_equal(desc[:, 6], (re - rs + 255) // 256)
     slot = np.arange(nch)
     assert np.all((desc[:, 5] <= slot) & (slot < desc[:, 5] + desc[:, 6]))
@@ -262,7 +263,7 @@ def test_chunk_descriptors_and_window_order(B):
     assert len(np.unique(desc[:, 4])) == res["num_long"]
     if B >= 4096:
         # key = table * windows per table + (first bag >> 9): payload = bag
-        np.testing.assert_array_equal(desc[:, 7], desc[:, 3] * ((B + 511) // 512) + (vals[desc[:, 0]] >> 9))
+        np.testing.assert_array_equal(desc[:, 7], table * ((B + 511) // 512) + (vals[desc[:, 0]] >> 9))
         np.testing.assert_array_equal(np.sort(order), slot)
         assert np.all(np.diff(desc[order, 7]) >= 0)
     else:
