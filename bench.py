@@ -512,85 +512,146 @@ def run_ours(args):
 
 
 def run_e2e(args, wl, tables, tbe, cfg, idx_h, off_h, G_h, psw_h, wt, mom, dev, world):
-    """Same step through the public API from pinned host memory: every step
-    uploads its batch (indices, offsets, weights) and upstream gradient and
-    downloads its pooled output.  Uploads run on one copy stream and downloads
-    on another, into double-buffered device tensors, so step i+1's upload and
-    step i's download overlap step i's compute."""
+    """The step through the public API from pinned host memory.  Every step
+    uploads its inputs -- the batch (indices, offsets, weights) and the
+    upstream gradient of the pooled output -- and reads back its result on
+    the host: the status words (out-of-range count and error flags), which a
+    caller must check after every step.  Uploads run on one copy stream and
+    the read-back on another, into double-buffered device tensors, so step
+    i+1's upload overlaps step i's compute.  The pipeline of all the timed
+    steps is captured once as a CUDA graph (the same calls, enqueued ahead),
+    so host speed does not pace it.  A second figure also downloads each
+    step's pooled output [B, T*D] (the forward's activations)."""
     import torch
     from recsys_table_embedding_gb300 import Batch
     idx_p, off_p, G_p = idx_h.pin_memory(), off_h.pin_memory(), G_h.pin_memory()
     psw_p = psw_h.pin_memory() if psw_h is not None else None
+    steps = max(3, min(args.steps, 10))
     out_p = [torch.empty((wl.B, wl.T * wl.D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    stat_p = torch.zeros((steps, 4), dtype=torch.int32).pin_memory()
     bufs = []
     for _ in range(2):
         idx_d, off_d = torch.empty_like(idx_h, device=dev), torch.empty_like(off_h, device=dev)
         psw_d = torch.empty_like(psw_h, device=dev) if psw_h is not None else None
         bufs.append(dict(idx=idx_d, off=off_d, psw=psw_d, G=torch.empty_like(G_h, device=dev),
                          out=torch.empty((wl.B, wl.T * wl.D), dtype=torch.float32, device=dev),
-                         batch=Batch(idx_d, off_d, wl.B, psw_d, wt),
-                         bwd_done=None, out_copied=None))
-    main = torch.cuda.current_stream(dev)
+                         batch=Batch(idx_d, off_d, wl.B, psw_d, wt)))
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    h2d = idx_h.numel() * 4 + off_h.numel() * 4 + G_h.numel() * 4 + (psw_h.numel() * 4 if psw_h is not None else 0)
-    d2h = out_p[0].numel() * 4
+    h2d = (idx_h.numel() * idx_h.element_size() + off_h.numel() * off_h.element_size()
+           + G_h.numel() * 4 + (psw_h.numel() * 4 if psw_h is not None else 0))
+    d2h_status = 4 * 4
+    d2h_out = out_p[0].numel() * 4
 
-    def e2e_step(i):
-        bf = bufs[i & 1]
-        # buffers of step i-2: its backward read G and the batch, its download read out
-        with torch.cuda.stream(up):
-            if bf["bwd_done"] is not None:
-                up.wait_event(bf["bwd_done"])
-            bf["idx"].copy_(idx_p, non_blocking=True)
-            bf["off"].copy_(off_p, non_blocking=True)
-            if bf["psw"] is not None:
-                bf["psw"].copy_(psw_p, non_blocking=True)
-            in_ready = torch.cuda.Event()
-            in_ready.record(up)
-            bf["G"].copy_(G_p, non_blocking=True)
-            g_ready = torch.cuda.Event()
-            g_ready.record(up)
-        main.wait_event(in_ready)
-        if bf["out_copied"] is not None:
-            main.wait_event(bf["out_copied"])
-        tbe.forward(bf["batch"], bf["out"])
-        fwd_done = torch.cuda.Event()
-        fwd_done.record(main)
-        with torch.cuda.stream(down):
-            down.wait_event(fwd_done)
-            out_p[i & 1].copy_(bf["out"], non_blocking=True)
-            out_copied = torch.cuda.Event()
-            out_copied.record(down)
-        main.wait_event(g_ready)
-        tbe.backward(bf["batch"], mom, bf["G"], wl.lr, wl.eps)
-        bwd_done = torch.cuda.Event()
-        bwd_done.record(main)
-        bf["bwd_done"], bf["out_copied"] = bwd_done, out_copied
-        return out_copied
+    def pipeline(main, with_out):
+        """Enqueue `steps` end-to-end steps; returns after joining the copy
+        streams back into `main`."""
+        fork = torch.cuda.Event()
+        fork.record(main)
+        up.wait_event(fork)
+        down.wait_event(fork)
+        state = [dict(bwd_done=None, out_copied=None) for _ in range(2)]
+        last_down = None
+        for i in range(steps):
+            bf, sv = bufs[i & 1], state[i & 1]
+            # buffers of step i-2: its backward read G and the batch, its
+            # download read out
+            with torch.cuda.stream(up):
+                if sv["bwd_done"] is not None:
+                    up.wait_event(sv["bwd_done"])
+                bf["idx"].copy_(idx_p, non_blocking=True)
+                bf["off"].copy_(off_p, non_blocking=True)
+                if bf["psw"] is not None:
+                    bf["psw"].copy_(psw_p, non_blocking=True)
+                in_ready = torch.cuda.Event()
+                in_ready.record(up)
+                bf["G"].copy_(G_p, non_blocking=True)
+                g_ready = torch.cuda.Event()
+                g_ready.record(up)
+            main.wait_event(in_ready)
+            if sv["out_copied"] is not None:
+                main.wait_event(sv["out_copied"])
+            tbe.forward(bf["batch"], bf["out"], stream=main)
+            if with_out:
+                fwd_done = torch.cuda.Event()
+                fwd_done.record(main)
+                with torch.cuda.stream(down):
+                    down.wait_event(fwd_done)
+                    out_p[i & 1].copy_(bf["out"], non_blocking=True)
+                    oc = torch.cuda.Event()
+                    oc.record(down)
+                sv["out_copied"] = oc
+            main.wait_event(g_ready)
+            tbe.backward(bf["batch"], mom, bf["G"], wl.lr, wl.eps, stream=main)
+            bwd_done = torch.cuda.Event()
+            bwd_done.record(main)
+            sv["bwd_done"] = bwd_done
+            with torch.cuda.stream(down):
+                down.wait_event(bwd_done)
+                stat_p[i].copy_(tbe.status, non_blocking=True)
+                last_down = torch.cuda.Event()
+                last_down.record(down)
+        last_up = torch.cuda.Event()
+        last_up.record(up)
+        main.wait_event(last_up)
+        main.wait_event(last_down)     # the last step's result is on the host
 
-    steps = max(3, min(args.steps, 10))
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    for bf in bufs:
-        bf["bwd_done"] = bf["out_copied"] = None
-    if world > 1:
-        torch.distributed.barrier()
+    def measure(with_out):
+        main = torch.cuda.current_stream(dev)
+        graph, mode = None, "cuda_graph"
+        if not args.eager:
+            try:
+                cap = torch.cuda.Stream(dev)
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+                    pipeline(torch.cuda.current_stream(dev), with_out)
+                graph.replay()          # upload and warm
+            except Exception as e:
+                graph, mode = None, f"eager (graph capture failed: {type(e).__name__}: {str(e)[:120]})"
+        else:
+            mode = "eager"
+        if graph is None:
+            pipeline(main, with_out)   # warm
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
+        a.record(main)
+        if graph is not None:
+            graph.replay()
+        else:
+            pipeline(main, with_out)
+        b.record(main)
+        host = (time.perf_counter() - h0) * 1e3
+        torch.cuda.synchronize(dev)
+        return reduce_max(a.elapsed_time(b), dev, world), mode, host
+
+    ms, mode, host = measure(False)
+    res = {"value": round(wl.N * world * steps / (ms / 1e3), 1), "unit": UNIT,
+           "ms_per_step": round(ms / steps, 4), "steps": steps,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h_status),
+           "launch_mode": mode, "host_enqueue_ms_per_step": round(host / steps, 4),
+           "result_read_back": "status words (out-of-range count, error flags) of every step",
+           "pipeline": "uploads and read-backs on two copy streams, double-buffered, overlapping compute"}
+    ms2, _, _ = measure(True)
+    res["with_output_download"] = {"value": round(wl.N * world * steps / (ms2 / 1e3), 1),
+                                   "ms_per_step": round(ms2 / steps, 4),
+                                   "d2h_bytes_per_step": int(d2h_status + d2h_out)}
+    # copy rates alone, for reading the figures above
+    x = torch.empty_like(G_h, device=dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(main)
-    up.wait_event(a)
-    down.wait_event(a)
-    last = None
-    for i in range(steps):
-        last = e2e_step(i)
-    main.wait_event(last)      # the last step's output is on the host
-    b.record(main)
+    a.record()
+    x.copy_(G_p, non_blocking=True)
+    b.record()
     torch.cuda.synchronize(dev)
-    ms = reduce_max(a.elapsed_time(b), dev, world)
-    return {"value": round(wl.N * world * steps / (ms / 1e3), 1), "unit": UNIT,
-            "ms_per_step": round(ms / steps, 4), "steps": steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipeline": "uploads and downloads on two copy streams, double-buffered, overlapping compute"}
+    res["h2d_gbs"] = round(G_h.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+    a.record()
+    out_p[0].copy_(bufs[0]["out"], non_blocking=True)
+    b.record()
+    torch.cuda.synchronize(dev)
+    res["d2h_gbs"] = round(d2h_out / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+    del x
+    return res
 
 
 # ----------------------------------------------------------------- oracle
