@@ -44,19 +44,19 @@ def lib():
         i32, i64, f32, f64, u16 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                    ctypes.c_double, ctypes.c_uint16)
         L.tbe_oracle_forward.restype = i64
-        L.tbe_oracle_forward.argtypes = [i32, i64, i32, i32, P, P, P, P, i64, P, P, P, i64, P, P, P]
+        L.tbe_oracle_forward.argtypes = [i32, i64, P, i32, P, P, P, P, i64, P, P, P, i64, P, P, P]
         L.tbe_oracle_preprocess.restype = i64
-        L.tbe_oracle_preprocess.argtypes = [i32, i64, P, P, P, i64, P, P, P, P, P, P]
+        L.tbe_oracle_preprocess.argtypes = [i32, i64, P, P, P, P, i64, P, P, P, P, P, P]
         L.tbe_oracle_backward_adagrad.restype = i64
-        L.tbe_oracle_backward_adagrad.argtypes = [i32, i64, i32, i32, P, P, P, P, P, i64, P, P, P,
+        L.tbe_oracle_backward_adagrad.argtypes = [i32, i64, P, i32, P, P, P, P, P, i64, P, P, P,
                                                   f32, f32, P, P, P]
         L.tbe_oracle_rows_update.restype = i64
-        L.tbe_oracle_rows_update.argtypes = [i32, i64, i32, i32, P, P, P, i64, P, P, P, f32, f32, P,
-                                             i64, P, P, P, P, P]
+        L.tbe_oracle_rows_update.argtypes = [i32, i64, P, i32, P, P, P, i64, P, P, P, f32, f32, P,
+                                             i64, P, i64, P, P, P, P]
         L.tbe_oracle_histogram.restype = i64
-        L.tbe_oracle_histogram.argtypes = [i32, i64, i32, P, P, P, i64, P]
+        L.tbe_oracle_histogram.argtypes = [i32, i64, P, i32, P, P, P, i64, P]
         L.tbe_oracle_offsets_check.restype = i32
-        L.tbe_oracle_offsets_check.argtypes = [i32, i64, P, i64, P, P, P]
+        L.tbe_oracle_offsets_check.argtypes = [i64, P, i64, P, P, P]
         for n in ("tbe_oracle_to_half", "tbe_oracle_to_bf16"):
             getattr(L, n).restype = u16
             getattr(L, n).argtypes = [f64]
@@ -75,39 +75,61 @@ def _c(a, dtype):
     return None if a is None else np.ascontiguousarray(a, dtype=dtype)
 
 
-def _wbits(W: np.ndarray, dtype: str) -> np.ndarray:
-    """Weights as raw storage: float32 array for f32, uint16 bit patterns for f16/bf16."""
-    if dtype == "f32":
-        return np.ascontiguousarray(W, dtype=np.float32)
-    assert W.dtype == np.uint16, "f16/bf16 weights are passed as uint16 bit patterns"
-    return np.ascontiguousarray(W)
+class _Problem:
+    """The batch and table description of a workload as the C oracle takes
+    it; the widened arrays are held here while a call reads them."""
+
+    def __init__(self, wl):
+        self.T, self.NB, self.N = wl.T, wl.NB, wl.N
+        self.Dmax = wl.Dmax
+        self.layout = np.array([[L["wbyte"], L["out_off"], L["stride"], L["bag_off"], L["B"], L["D"],
+                                 DTYPE_CODE[L["dtype"]]] for L in wl.layout()], np.int64)
+        self.to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
+        self.idx = _c(wl.indices, np.int64)
+        self.off = _c(wl.offsets, np.int64)
+        self.psw = _c(wl.per_sample_weights, np.float32)
+        self.wt = _c(wl.weighted_tables, np.uint8)
+
+
+def _wbytes(W: np.ndarray, wl) -> np.ndarray:
+    """Weights as raw storage bytes: a float32 array for f32 tables, uint16 bit
+    patterns for f16/bf16 tables, or the byte buffer of tables of different
+    shapes."""
+    if not wl.mixed:
+        if wl.dtype == "f32":
+            W = np.ascontiguousarray(W, dtype=np.float32)
+        else:
+            assert W.dtype == np.uint16, "f16/bf16 weights are passed as uint16 bit patterns"
+            W = np.ascontiguousarray(W)
+    else:
+        assert W.dtype == np.uint8, "tables of different shapes pass their weights as bytes"
+        W = np.ascontiguousarray(W)
+    return W
 
 
 def forward(wl, W: np.ndarray, bags: Optional[np.ndarray] = None, want_abs: bool = False):
     """Pooled forward.  Returns (out, abs_sum|None, oob, bad_bags).
 
     ``W`` is the flat [rows_total, D] table store (float32, or uint16 bits for
-    f16/bf16).  With ``bags`` (int64 bag ids t*B+b) out is [len(bags), D].
+    f16/bf16; a byte buffer for tables of different shapes).  out is
+    [B, T*D] ([out_size] for tables of different shapes); with ``bags``
+    (CSR bag ids) it is [len(bags), Dmax].
     """
     L = lib()
-    W = _wbits(W, wl.dtype)
-    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
-    idx = _c(wl.indices, np.int64)
-    off = _c(wl.offsets, np.int64)
-    psw = _c(wl.per_sample_weights, np.float32)
-    wt = _c(wl.weighted_tables, np.uint8)
+    pr = _Problem(wl)
+    W = _wbytes(W, wl)
     if bags is None:
-        out = np.zeros((wl.B, wl.T * wl.D), dtype=np.float32)
+        out = np.zeros(wl.out_size if wl.mixed else (wl.B, wl.T * wl.D), dtype=np.float32)
         nb = 0
     else:
         bags = np.ascontiguousarray(bags, dtype=np.int64)
-        out = np.zeros((len(bags), wl.D), dtype=np.float32)
+        out = np.zeros((len(bags), pr.Dmax), dtype=np.float32)
         nb = len(bags)
     ab = np.zeros(out.shape, dtype=np.float64) if want_abs else None
     bad = ctypes.c_int64(0)
-    oob = L.tbe_oracle_forward(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(to), _p(idx),
-                               _p(off), wl.N, _p(psw), _p(wt), _p(bags), nb, _p(out), _p(ab),
-                               ctypes.addressof(bad))
+    oob = L.tbe_oracle_forward(pr.T, pr.NB, _p(pr.layout), pr.Dmax, _p(W), _p(pr.to), _p(pr.idx),
+                               _p(pr.off), pr.N, _p(pr.psw), _p(pr.wt), _p(bags), nb, _p(out),
+                               _p(ab), ctypes.addressof(bad))
     return out, ab, int(oob), int(bad.value)
 
 
@@ -115,17 +137,16 @@ def preprocess(wl):
     """Batch inversion.  Returns dict of sorted_keys, sorted_pos, unique_keys,
     run_len, seg_off (int64) and num_unique, n_valid."""
     L = lib()
+    pr = _Problem(wl)
     N = wl.N
-    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
     sk = np.zeros(max(N, 1), np.int64)
     sp = np.zeros(max(N, 1), np.int64)
     uk = np.zeros(max(N, 1), np.int64)
     rl = np.zeros(max(N, 1), np.int64)
     so = np.zeros(N + 1, np.int64)
     nv = ctypes.c_int64(0)
-    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
-    U = L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(idx), _p(off), N, _p(sk), _p(sp), _p(uk),
-                                _p(rl), _p(so), ctypes.addressof(nv))
+    U = L.tbe_oracle_preprocess(pr.T, pr.NB, _p(pr.layout), _p(pr.to), _p(pr.idx), _p(pr.off), N,
+                                _p(sk), _p(sp), _p(uk), _p(rl), _p(so), ctypes.addressof(nv))
     nv = int(nv.value)
     return dict(sorted_keys=sk[:nv], sorted_pos=sp[:nv], unique_keys=uk[:U], run_len=rl[:U],
                 seg_off=so[:U + 1], num_unique=int(U), n_valid=nv)
@@ -134,10 +155,9 @@ def preprocess(wl):
 def num_runs(wl) -> int:
     """Number of runs (unique touched rows) of the batch inversion."""
     L = lib()
-    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
-    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
-    return int(L.tbe_oracle_preprocess(wl.T, wl.B, _p(to), _p(idx), _p(off), wl.N, None, None, None,
-                                       None, None, None))
+    pr = _Problem(wl)
+    return int(L.tbe_oracle_preprocess(pr.T, pr.NB, _p(pr.layout), _p(pr.to), _p(pr.idx), _p(pr.off),
+                                       pr.N, None, None, None, None, None, None))
 
 
 def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarray,
@@ -146,34 +166,31 @@ def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarr
     """Backward + exact rowwise Adagrad, in place on copies.
 
     Returns (W_new, momentum_new, U, row_grad|None, update_count|None);
-    row_grad is dense [rows_total, D] (small problems only).  With
+    row_grad is dense [rows_total, Dmax] (small problems only).  With
     ``want_runs`` a sixth item is a dict of per-run arrays in ascending key
-    order: keys [U], grad [U, D] (the row gradient), abs [U, D] (the sum of
-    its terms' magnitudes) and count [U] (lookups of the run).
+    order: keys [U], grad [U, Dmax] (the row gradient), abs [U, Dmax] (the
+    sum of its terms' magnitudes) and count [U] (lookups of the run).
     """
     L = lib()
-    W = _wbits(W, wl.dtype).copy()
+    pr = _Problem(wl)
+    W = _wbytes(W, wl).copy()
     m = np.ascontiguousarray(momentum, dtype=np.float32).copy()
-    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
     go = np.ascontiguousarray(grad_out, dtype=np.float32)
     runs = None
     rg = ra = None
     if want_row_grad or want_runs:
         pre = preprocess(wl)
         U0 = pre["num_unique"]
-        rg = np.zeros((max(U0, 1), wl.D), np.float64)
-        ra = np.zeros((max(U0, 1), wl.D), np.float64)
+        rg = np.zeros((max(U0, 1), pr.Dmax), np.float64)
+        ra = np.zeros((max(U0, 1), pr.Dmax), np.float64)
         runs = dict(keys=pre["unique_keys"], grad=rg[:U0], abs=ra[:U0], count=pre["run_len"])
     uc = np.zeros(wl.rows_total, np.int32) if want_update_count else None
-    # widened copies are held in locals: the C call reads them
-    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
-    psw, wt = _c(wl.per_sample_weights, np.float32), _c(wl.weighted_tables, np.uint8)
-    U = L.tbe_oracle_backward_adagrad(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(W), _p(m), _p(to),
-                                      _p(idx), _p(off), wl.N, _p(psw), _p(wt), _p(go),
+    U = L.tbe_oracle_backward_adagrad(pr.T, pr.NB, _p(pr.layout), pr.Dmax, _p(W), _p(m), _p(pr.to),
+                                      _p(pr.idx), _p(pr.off), pr.N, _p(pr.psw), _p(pr.wt), _p(go),
                                       float(wl.lr), float(wl.eps), _p(rg), _p(ra), _p(uc))
     dense = None
     if want_row_grad:
-        dense = np.zeros((wl.rows_total, wl.D), np.float64)
+        dense = np.zeros((wl.rows_total, pr.Dmax), np.float64)
         dense[runs["keys"]] = runs["grad"]
     if want_runs:
         return W, m, int(U), dense, uc, runs
@@ -183,50 +200,52 @@ def backward_adagrad(wl, W: np.ndarray, momentum: np.ndarray, grad_out: np.ndarr
 def rows_update(wl, rows: np.ndarray, W_rows: np.ndarray, mom_rows: np.ndarray,
                 grad_out: np.ndarray, want_row_abs: bool = False):
     """Sampled-row backward: rows (sorted distinct linearised keys) with their
-    pre-update W rows and momentum.  Returns (W_rows_new, mom_new, row_grad,
-    counts, n_valid), plus row_abs as a sixth item when ``want_row_abs``."""
+    pre-update W rows ([k, D] float32, or uint16 bits; uniform tables) and
+    momentum.  Returns (W_rows_new, mom_new, row_grad, counts, n_valid), plus
+    row_abs as a sixth item when ``want_row_abs``."""
     L = lib()
+    assert not wl.mixed
+    pr = _Problem(wl)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     assert np.all(np.diff(rows) > 0)
     k = len(rows)
-    Wr = _wbits(W_rows, wl.dtype).copy()
+    Wr = _wbytes(W_rows, wl).copy()
+    row_bytes = wl.D * (4 if wl.dtype == "f32" else 2)
     mr = np.ascontiguousarray(mom_rows, dtype=np.float32).copy()
     rg = np.zeros((k, wl.D), np.float64)
     ra = np.zeros((k, wl.D), np.float64) if want_row_abs else None
     cnt = np.zeros(k, np.int64)
-    to = np.ascontiguousarray(wl.table_offset, dtype=np.int64)
-    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
-    psw, wt = _c(wl.per_sample_weights, np.float32), _c(wl.weighted_tables, np.uint8)
     go = np.ascontiguousarray(grad_out, dtype=np.float32)
-    nv = L.tbe_oracle_rows_update(wl.T, wl.B, wl.D, DTYPE_CODE[wl.dtype], _p(to), _p(idx), _p(off),
-                                  wl.N, _p(psw), _p(wt), _p(go), float(wl.lr), float(wl.eps),
-                                  _p(rows), k, _p(Wr), _p(mr), _p(rg), _p(ra), _p(cnt))
+    nv = L.tbe_oracle_rows_update(pr.T, pr.NB, _p(pr.layout), pr.Dmax, _p(pr.to), _p(pr.idx),
+                                  _p(pr.off), pr.N, _p(pr.psw), _p(pr.wt), _p(go), float(wl.lr),
+                                  float(wl.eps), _p(rows), k, _p(Wr), row_bytes, _p(mr), _p(rg),
+                                  _p(ra), _p(cnt))
     if want_row_abs:
         return Wr, mr, rg, cnt, int(nv), ra
     return Wr, mr, rg, cnt, int(nv)
 
 
 def histogram(wl, Emax: int = 64) -> np.ndarray:
-    """Per-bag row counts, int32 [T, B, Emax]."""
+    """Per-bag row counts, int32 [T, B, Emax] (uniform tables)."""
     L = lib()
+    pr = _Problem(wl)
     c = np.zeros((wl.T, wl.B, Emax), np.int32)
-    to = np.ascontiguousarray(wl.table_offset, np.int64)
-    idx, off = _c(wl.indices, np.int64), _c(wl.offsets, np.int64)
-    L.tbe_oracle_histogram(wl.T, wl.B, Emax, _p(to), _p(idx), _p(off), wl.N, _p(c))
+    L.tbe_oracle_histogram(pr.T, pr.NB, _p(pr.layout), Emax, _p(pr.to), _p(pr.idx), _p(pr.off), pr.N,
+                           _p(c))
     return c
 
 
 def offsets_check(wl):
     """(malformed, bad_bags, decreasing, span) of the batch's offsets: bags
     not 0 <= start <= end <= N, whether any bag has end < start, whether
-    offsets[0] != 0 or offsets[T*B] != N."""
+    offsets[0] != 0 or offsets[NB] != N."""
     L = lib()
     bad = ctypes.c_int64(0)
     dec = ctypes.c_int32(0)
     sp = ctypes.c_int32(0)
     off = _c(wl.offsets, np.int64)
-    m = L.tbe_oracle_offsets_check(wl.T, wl.B, _p(off), wl.N,
-                                   ctypes.addressof(bad), ctypes.addressof(dec), ctypes.addressof(sp))
+    m = L.tbe_oracle_offsets_check(wl.NB, _p(off), wl.N, ctypes.addressof(bad), ctypes.addressof(dec),
+                                   ctypes.addressof(sp))
     return bool(m), int(bad.value), bool(dec.value), bool(sp.value)
 
 

@@ -42,15 +42,34 @@
  * FP16/BF16 weights, FP64 for FP32 weights); the oracle is at least as
  * accurate as either, so a comparison measures the kernel's own rounding.
  *
+ * Tables and bags.  Table t owns linearised rows [table_offset[t],
+ * table_offset[t+1]) and is described by a layout record of 7 int64
+ * (layout[t*7 + k]):
+ *   k = 0  first byte of its rows in the weight buffer W (row r of the
+ *          table, element d: byte 0 + ((r - table_offset[t]) * D + d) * size)
+ *   k = 1  index in out / grad_out of bag 0's first element
+ *   k = 2  elements from one bag's row to the next in out / grad_out
+ *   k = 3  CSR bag index of its bag 0 (tables follow one another)
+ *   k = 4  B_t, its bags in this batch
+ *   k = 5  D_t, elements per row
+ *   k = 6  dtype of its weights
+ * One layout covers the uniform problem of the pages' notation (every table
+ * with the same D, dtype and B; out = [B, T*D]), tables of different D and
+ * dtype in one fused call (TorchEasyRec analysis, section 1: one lookup for
+ * all features of a KeyedJagged batch), and variable batch size per table
+ * (VBE, which the FBTriton TBE redesign names in decision checklist item 5;
+ * read here as table t having its own B_t, its bags' rows packed one after
+ * another in out and grad_out).
+ *
  * Out-of-range indices (idx < 0 or idx >= E_t) are counted, contribute
  * nothing to the forward and take no part in the backward.
  *
  * Malformed offsets (the pages say nothing about them; this is the reading
  * both sides implement):
- *  - a bag (t,b) is well formed when 0 <= offsets[g] <= offsets[g+1] <= N
- *    (g = t*B + b); any other bag is malformed, counted, and empty;
+ *  - a bag g is well formed when 0 <= offsets[g] <= offsets[g+1] <= N; any
+ *    other bag is malformed, counted, and empty;
  *  - lookups outside every well-formed bag (before offsets[0], after
- *    offsets[T*B], or inside a malformed bag) take no part in the forward or
+ *    offsets[NB], or inside a malformed bag) take no part in the forward or
  *    the backward;
  *  - offsets that decrease anywhere (some bag with end < start) leave no
  *    single bag for a lookup that two well-formed bags both cover, so such a
@@ -160,6 +179,7 @@ static void store_w(void *W, int dtype, int64_t i, double v)
         ((uint16_t *)W)[i] = double_to_bf16_bits(v);
 }
 
+
 /* exported for the conversion pins */
 uint16_t tbe_oracle_to_half(double x) { return double_to_half_bits(x); }
 uint16_t tbe_oracle_to_bf16(double x) { return double_to_bf16_bits(x); }
@@ -167,6 +187,36 @@ double tbe_oracle_from_half(uint16_t h) { return half_bits_to_double(h); }
 double tbe_oracle_from_bf16(uint16_t h) { return bf16_bits_to_double(h); }
 
 /* ------------------------------------------------------------------ */
+/* Tables                                                              */
+
+#define LAY(t, k) layout[(int64_t)(t) * 7 + (k)]
+
+static int64_t elem_size(int64_t dtype) { return dtype == 0 ? 4 : 2; }
+
+/* byte address of element 0 of linearised row `row` of table t */
+static unsigned char *row_ptr(const void *W, const int64_t *layout, const int64_t *table_offset,
+                              int64_t t, int64_t row)
+{
+    return (unsigned char *)W + LAY(t, 0) + (row - table_offset[t]) * LAY(t, 5) * elem_size(LAY(t, 6));
+}
+
+/* table of CSR bag g: the t with LAY(t,3) <= g < LAY(t,3) + LAY(t,4) */
+static int64_t table_of_bag(const int64_t *layout, int32_t T, int64_t g)
+{
+    for (int64_t t = 0; t < T; ++t)
+        if (g >= LAY(t, 3) && g < LAY(t, 3) + LAY(t, 4))
+            return t;
+    return -1;
+}
+
+/* table of linearised row `row` */
+static int64_t table_of_row(const int64_t *table_offset, int32_t T, int64_t row)
+{
+    int64_t t = 0;
+    while (t + 1 < T && table_offset[t + 1] <= row)
+        ++t;
+    return t;
+}
 
 static double sample_weight(const float *psw, const uint8_t *weighted, int64_t t, int64_t p)
 {
@@ -177,37 +227,44 @@ static double sample_weight(const float *psw, const uint8_t *weighted, int64_t t
     return (double)psw[p];
 }
 
+static int well_formed(const int64_t *offsets, int64_t g, int64_t N)
+{
+    int64_t s = offsets[g], e = offsets[g + 1];
+    return 0 <= s && s <= e && e <= N;
+}
+
 /*
- * Forward pooled sum for a list of bags (all T*B bags when bags == NULL).
+ * Forward pooled sum for a list of bags (all NB bags when bags == NULL).
  *
- *   out[b, t*D + d] = sum_{p in bag (t,b), 0 <= idx_p < E_t} w_p * W[table_offset[t] + idx_p, d]
+ *   out[row of bag (t,b) + d] = sum_{p in bag, 0 <= idx_p < E_t} w_p * W_t[idx_p, d]
  *
- * indices[N] and offsets[T*B+1] are int64 here (the caller widens int32
- * inputs).  With bags == NULL the output is the full [B, T*D] matrix; with a
- * bag list row k of out ([nbags, D]) belongs to bag bags[k] = t*B + b.
- * abs_sum (nullable) receives sum |w_p * W[.., d]| in the same layout: the
- * scale that bounds any summation-order rounding of out.
+ * indices[N] and offsets[NB+1] are int64 (callers widen int32 inputs).  With
+ * bags == NULL bag (t,b) writes its D_t elements at out[LAY(t,1) +
+ * b*LAY(t,2) + d]; with a bag list, row k of out ([nbags, Dmax]) belongs to
+ * bags[k].  abs_sum (nullable) receives sum |w_p * W[.., d]| in the same
+ * layout: the scale that bounds any summation-order rounding of out.
  * Returns the number of out-of-range lookups in the bags visited;
  * *bad_bags (nullable) the number of malformed bags among them.
  */
-int64_t tbe_oracle_forward(int32_t T, int64_t B, int32_t D, int32_t dtype, const void *W,
-                           const int64_t *table_offset, const int64_t *indices,
+int64_t tbe_oracle_forward(int32_t T, int64_t NB, const int64_t *layout, int32_t Dmax,
+                           const void *W, const int64_t *table_offset, const int64_t *indices,
                            const int64_t *offsets, int64_t N, const float *psw,
                            const uint8_t *weighted, const int64_t *bags, int64_t nbags,
                            float *out, double *abs_sum, int64_t *bad_bags)
 {
     int64_t oob = 0, bad = 0;
-    int64_t n = bags ? nbags : (int64_t)T * B;
-    double *acc = (double *)malloc(sizeof(double) * (size_t)D);
-    double *aab = (double *)malloc(sizeof(double) * (size_t)D);
+    int64_t n = bags ? nbags : NB;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)Dmax);
+    double *aab = (double *)malloc(sizeof(double) * (size_t)Dmax);
     for (int64_t k = 0; k < n; ++k) {
-        int64_t bag = bags ? bags[k] : k;
-        int64_t t = bag / B, b = bag % B;
+        int64_t g = bags ? bags[k] : k;
+        int64_t t = table_of_bag(layout, T, g), b = g - LAY(t, 3);
         int64_t E = table_offset[t + 1] - table_offset[t];
-        for (int d = 0; d < D; ++d)
+        int64_t D = LAY(t, 5), dtype = LAY(t, 6);
+        for (int64_t d = 0; d < D; ++d)
             acc[d] = aab[d] = 0.0;
-        int64_t start = offsets[bag], end = offsets[bag + 1];
-        if (!(0 <= start && start <= end && end <= N)) {
+        int64_t start = offsets[g], end = offsets[g + 1];
+        if (!well_formed(offsets, g, N)) {
             ++bad;                       /* malformed bag: empty */
             start = end = 0;
         }
@@ -218,15 +275,15 @@ int64_t tbe_oracle_forward(int32_t T, int64_t B, int32_t D, int32_t dtype, const
                 continue;
             }
             double w = sample_weight(psw, weighted, t, p);
-            int64_t row = table_offset[t] + idx;
-            for (int d = 0; d < D; ++d) {
-                double v = w * load_w(W, dtype, row * D + d);
+            const unsigned char *wr = row_ptr(W, layout, table_offset, t, table_offset[t] + idx);
+            for (int64_t d = 0; d < D; ++d) {
+                double v = w * load_w(wr, (int)dtype, d);
                 acc[d] += v;
                 aab[d] += fabs(v);
             }
         }
-        int64_t o = bags ? k * D : (b * T + t) * D;
-        for (int d = 0; d < D; ++d) {
+        int64_t o = bags ? k * Dmax : LAY(t, 1) + b * LAY(t, 2);
+        for (int64_t d = 0; d < D; ++d) {
             out[o + d] = (float)acc[d];
             if (abs_sum)
                 abs_sum[o + d] = aab[d];
@@ -260,19 +317,18 @@ static int cmp_key_pos(const void *a, const void *b)
 /*
  * Shape of the offsets array: *bad_bags = malformed bags (not
  * 0 <= offsets[g] <= offsets[g+1] <= N), *decreasing = 1 when some bag has
- * end < start, *span = 1 when offsets[0] != 0 or offsets[T*B] != N.
+ * end < start, *span = 1 when offsets[0] != 0 or offsets[NB] != N.
  * Returns 1 when any of the three holds (the batch's offsets are malformed).
  */
-int32_t tbe_oracle_offsets_check(int32_t T, int64_t B, const int64_t *offsets, int64_t N,
+int32_t tbe_oracle_offsets_check(int64_t NB, const int64_t *offsets, int64_t N,
                                  int64_t *bad_bags, int32_t *decreasing, int32_t *span)
 {
-    int64_t NB = (int64_t)T * B, bad = 0;
+    int64_t bad = 0;
     int32_t dec = 0;
     for (int64_t g = 0; g < NB; ++g) {
-        int64_t s = offsets[g], e = offsets[g + 1];
-        if (e < s)
+        if (offsets[g + 1] < offsets[g])
             dec = 1;
-        if (!(0 <= s && s <= e && e <= N))
+        if (!well_formed(offsets, g, N))
             ++bad;
     }
     int32_t sp = offsets[0] != 0 || offsets[NB] != N;
@@ -286,24 +342,23 @@ int32_t tbe_oracle_offsets_check(int32_t T, int64_t B, const int64_t *offsets, i
 }
 
 /*
- * Bag id (t*B + b) of every position p for the backward; -1 for positions in
- * no well-formed bag.  Offsets that decrease anywhere give -1 everywhere
- * (such a batch has no backward update).
+ * CSR bag of every position p for the backward; -1 for positions in no
+ * well-formed bag.  Offsets that decrease anywhere give -1 everywhere (such
+ * a batch has no backward update).
  */
-static int64_t *bag_of_positions(int32_t T, int64_t B, const int64_t *offsets, int64_t N)
+static int64_t *bag_of_positions(int64_t NB, const int64_t *offsets, int64_t N)
 {
     int64_t *bag = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     for (int64_t p = 0; p < N; ++p)
         bag[p] = -1;
     int32_t dec = 0;
-    tbe_oracle_offsets_check(T, B, offsets, N, NULL, &dec, NULL);
+    tbe_oracle_offsets_check(NB, offsets, N, NULL, &dec, NULL);
     if (dec)
         return bag;
-    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
-        int64_t s = offsets[g], e = offsets[g + 1];
-        if (!(0 <= s && s <= e && e <= N))
+    for (int64_t g = 0; g < NB; ++g) {
+        if (!well_formed(offsets, g, N))
             continue;
-        for (int64_t p = s; p < e; ++p)
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p)
             bag[p] = g;
     }
     return bag;
@@ -311,25 +366,26 @@ static int64_t *bag_of_positions(int32_t T, int64_t B, const int64_t *offsets, i
 
 /*
  * key_p = table_offset[t] + idx_p for every in-range lookup p of a
- * well-formed bag (t its table; see bag_of_positions),
- * sorted by (key, p) -- a stable sort by key -- then run-length encoded:
+ * well-formed bag (t its table; see bag_of_positions), sorted by (key, p)
+ * -- a stable sort by key -- then run-length encoded:
  *   unique_keys[r], run_len[r], seg_off[r] (exclusive prefix sum of run_len,
  *   seg_off[U] = N' = number of in-range lookups).
  * sorted_keys/sorted_pos have N' entries.  Any output may be NULL.
  * Returns U.
  */
-int64_t tbe_oracle_preprocess(int32_t T, int64_t B, const int64_t *table_offset,
-                              const int64_t *indices, const int64_t *offsets, int64_t N,
-                              int64_t *sorted_keys, int64_t *sorted_pos, int64_t *unique_keys,
-                              int64_t *run_len, int64_t *seg_off, int64_t *n_valid)
+int64_t tbe_oracle_preprocess(int32_t T, int64_t NB, const int64_t *layout,
+                              const int64_t *table_offset, const int64_t *indices,
+                              const int64_t *offsets, int64_t N, int64_t *sorted_keys,
+                              int64_t *sorted_pos, int64_t *unique_keys, int64_t *run_len,
+                              int64_t *seg_off, int64_t *n_valid)
 {
-    int64_t *bag = bag_of_positions(T, B, offsets, N);
+    int64_t *bag = bag_of_positions(NB, offsets, N);
     kp_t *kp = (kp_t *)malloc(sizeof(kp_t) * (size_t)(N > 0 ? N : 1));
     int64_t nv = 0;
     for (int64_t p = 0; p < N; ++p) {
         if (bag[p] < 0)
             continue;
-        int64_t t = bag[p] / B;
+        int64_t t = table_of_bag(layout, T, bag[p]);
         int64_t E = table_offset[t + 1] - table_offset[t];
         int64_t idx = indices[p];
         if (idx < 0 || idx >= E)
@@ -367,36 +423,39 @@ int64_t tbe_oracle_preprocess(int32_t T, int64_t B, const int64_t *table_offset,
 /* ------------------------------------------------------------------ */
 /* Backward with the fused exact rowwise Adagrad update.                 */
 
-/* One exact rowwise Adagrad step on row `row` with row gradient g[0..D). */
-static void adagrad_row(void *W, float *momentum, int32_t D, int32_t dtype, int64_t row,
-                        const double *g, float lr, float eps)
+/* One exact rowwise Adagrad step on one row (D elements of dtype at wr,
+ * its momentum *m) with row gradient g[0..D). */
+static void adagrad_row(unsigned char *wr, float *m, int64_t D, int dtype, const double *g,
+                        float lr, float eps)
 {
     double ss = 0.0;
-    for (int d = 0; d < D; ++d)
+    for (int64_t d = 0; d < D; ++d)
         ss += g[d] * g[d];
-    momentum[row] = (float)((double)momentum[row] + ss / (double)D);
-    double den = sqrt((double)momentum[row]) + (double)eps;
-    for (int d = 0; d < D; ++d) {
-        double w = load_w(W, dtype, row * D + d);
-        store_w(W, dtype, row * D + d, w - (double)lr * g[d] / den);
+    *m = (float)((double)*m + ss / (double)D);
+    double den = sqrt((double)*m) + (double)eps;
+    for (int64_t d = 0; d < D; ++d) {
+        double w = load_w(wr, dtype, d);
+        store_w(wr, dtype, d, w - (double)lr * g[d] / den);
     }
 }
 
 /*
  * Full backward in the pages' order: batch inversion (linearise, stable
- * sort, RLE), then for every run r (one unique row) the row gradient
- *     g[d] = sum_{p in run r, sorted order} w_p * grad_out[b(p), t*D + d]
- * and exactly one Adagrad update of that row.  W and momentum are updated in
- * place; rows no in-range lookup touches are not written.
- * run_grad (nullable, [U, D]) receives g of run r (rows in ascending key
+ * sort, RLE), then for every run r (one unique row of table t) the row
+ * gradient
+ *     g[d] = sum_{p in run r, sorted order} w_p * grad_out[row of bag(p) + d]
+ * and exactly one Adagrad update of that row.  W (bytes, laid out as the
+ * layout says) and momentum are updated in place; rows no in-range lookup
+ * touches are not written.
+ * run_grad (nullable, [U, Dmax]) receives g of run r (rows in ascending key
  * order, the order of tbe_oracle_preprocess's unique_keys); run_abs
- * (nullable, [U, D]) the sum |w_p * grad_out[..]| of the same terms (the
+ * (nullable, [U, Dmax]) the sum |w_p * grad_out[..]| of the same terms (the
  * scale that bounds a summation-order rounding of g); update_count
  * (nullable, [rows_total]) counts updates applied per row.
  * Returns U, the number of rows updated.
  */
-int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dtype, void *W,
-                                    float *momentum, const int64_t *table_offset,
+int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t NB, const int64_t *layout, int32_t Dmax,
+                                    void *W, float *momentum, const int64_t *table_offset,
                                     const int64_t *indices, const int64_t *offsets, int64_t N,
                                     const float *psw, const uint8_t *weighted,
                                     const float *grad_out, float lr, float eps,
@@ -406,32 +465,35 @@ int64_t tbe_oracle_backward_adagrad(int32_t T, int64_t B, int32_t D, int32_t dty
     int64_t *spos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     int64_t *ukeys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     int64_t *soff = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N + 1));
-    int64_t U = tbe_oracle_preprocess(T, B, table_offset, indices, offsets, N, skeys, spos, ukeys,
-                                      NULL, soff, NULL);
-    int64_t *bag = bag_of_positions(T, B, offsets, N);
-    double *g = (double *)malloc(sizeof(double) * (size_t)D);
-    double *ga = (double *)malloc(sizeof(double) * (size_t)D);
+    int64_t U = tbe_oracle_preprocess(T, NB, layout, table_offset, indices, offsets, N, skeys, spos,
+                                      ukeys, NULL, soff, NULL);
+    int64_t *bag = bag_of_positions(NB, offsets, N);
+    double *g = (double *)malloc(sizeof(double) * (size_t)Dmax);
+    double *ga = (double *)malloc(sizeof(double) * (size_t)Dmax);
     for (int64_t r = 0; r < U; ++r) {
         int64_t row = ukeys[r];
-        for (int d = 0; d < D; ++d)
+        int64_t t = table_of_row(table_offset, T, row);
+        int64_t D = LAY(t, 5);
+        for (int64_t d = 0; d < D; ++d)
             g[d] = ga[d] = 0.0;
         for (int64_t i = soff[r]; i < soff[r + 1]; ++i) {
             int64_t p = spos[i];
-            int64_t t = bag[p] / B, b = bag[p] % B;
+            int64_t b = bag[p] - LAY(t, 3);
             double w = sample_weight(psw, weighted, t, p);
-            const float *grow = grad_out + (b * T + t) * D;
-            for (int d = 0; d < D; ++d) {
+            const float *grow = grad_out + LAY(t, 1) + b * LAY(t, 2);
+            for (int64_t d = 0; d < D; ++d) {
                 g[d] += w * (double)grow[d];
                 ga[d] += fabs(w * (double)grow[d]);
             }
         }
         if (run_grad)
-            for (int d = 0; d < D; ++d)
-                run_grad[r * D + d] = g[d];
+            for (int64_t d = 0; d < D; ++d)
+                run_grad[r * Dmax + d] = g[d];
         if (run_abs)
-            for (int d = 0; d < D; ++d)
-                run_abs[r * D + d] = ga[d];
-        adagrad_row(W, momentum, D, dtype, row, g, lr, eps);
+            for (int64_t d = 0; d < D; ++d)
+                run_abs[r * Dmax + d] = ga[d];
+        adagrad_row(row_ptr(W, layout, table_offset, t, row), momentum + row, D, (int)LAY(t, 6), g,
+                    lr, eps);
         if (update_count)
             update_count[row] += 1;
     }
@@ -458,21 +520,22 @@ static int cmp_i64(const void *a, const void *b)
  * For k sampled linearised rows (sorted ascending, distinct) compute by one
  * scan over all lookups of the well-formed bags their lookup count, row
  * gradient (summed in position order, double; row_abs, nullable, the sum of
- * the terms' magnitudes) and the Adagrad result.  W_rows (dtype, [k, D]) and
- * mom_rows ([k]) hold the rows' values before the update and are updated in
- * place; rows with count 0 are left untouched.  row_grad ([k, D]) and counts
- * ([k]) are outputs.  Returns the number of in-range lookups scanned.
+ * the terms' magnitudes) and the Adagrad result.  W_rows ([k] rows of
+ * row_bytes bytes, each in its table's dtype and D) and mom_rows ([k]) hold
+ * the rows' values before the update and are updated in place; rows with
+ * count 0 are left untouched.  row_grad ([k, Dmax]) and counts ([k]) are
+ * outputs.  Returns the number of in-range lookups scanned.
  */
-int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
+int64_t tbe_oracle_rows_update(int32_t T, int64_t NB, const int64_t *layout, int32_t Dmax,
                                const int64_t *table_offset, const int64_t *indices,
                                const int64_t *offsets, int64_t N, const float *psw,
                                const uint8_t *weighted, const float *grad_out, float lr,
                                float eps, const int64_t *rows, int64_t k, void *W_rows,
-                               float *mom_rows, double *row_grad, double *row_abs,
-                               int64_t *counts)
+                               int64_t row_bytes, float *mom_rows, double *row_grad,
+                               double *row_abs, int64_t *counts)
 {
     int64_t nv = 0;
-    for (int64_t i = 0; i < k * D; ++i) {
+    for (int64_t i = 0; i < k * Dmax; ++i) {
         row_grad[i] = 0.0;
         if (row_abs)
             row_abs[i] = 0.0;
@@ -480,16 +543,16 @@ int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
     for (int64_t i = 0; i < k; ++i)
         counts[i] = 0;
     int32_t dec = 0;
-    tbe_oracle_offsets_check(T, B, offsets, N, NULL, &dec, NULL);
+    tbe_oracle_offsets_check(NB, offsets, N, NULL, &dec, NULL);
     if (dec)
         return 0;                        /* decreasing offsets: no update */
-    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
-        int64_t t = g / B, b = g % B;
-        int64_t E = table_offset[t + 1] - table_offset[t];
-        int64_t s = offsets[g], e = offsets[g + 1];
-        if (!(0 <= s && s <= e && e <= N))
+    for (int64_t g = 0; g < NB; ++g) {
+        if (!well_formed(offsets, g, N))
             continue;                    /* malformed bag */
-        for (int64_t p = s; p < e; ++p) {
+        int64_t t = table_of_bag(layout, T, g), b = g - LAY(t, 3);
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        int64_t D = LAY(t, 5);
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
             int64_t idx = indices[p];
             if (idx < 0 || idx >= E)
                 continue;
@@ -500,18 +563,22 @@ int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
                 continue;
             int64_t r = hit - rows;
             double w = sample_weight(psw, weighted, t, p);
-            const float *grow = grad_out + (b * T + t) * D;
-            for (int d = 0; d < D; ++d) {
-                row_grad[r * D + d] += w * (double)grow[d];
+            const float *grow = grad_out + LAY(t, 1) + b * LAY(t, 2);
+            for (int64_t d = 0; d < D; ++d) {
+                row_grad[r * Dmax + d] += w * (double)grow[d];
                 if (row_abs)
-                    row_abs[r * D + d] += fabs(w * (double)grow[d]);
+                    row_abs[r * Dmax + d] += fabs(w * (double)grow[d]);
             }
             counts[r] += 1;
         }
     }
-    for (int64_t s = 0; s < k; ++s)
-        if (counts[s] > 0)
-            adagrad_row(W_rows, mom_rows, D, dtype, s, row_grad + s * D, lr, eps);
+    for (int64_t r = 0; r < k; ++r) {
+        if (counts[r] == 0)
+            continue;
+        int64_t t = table_of_row(table_offset, T, rows[r]);
+        adagrad_row((unsigned char *)W_rows + r * row_bytes, mom_rows + r, LAY(t, 5), (int)LAY(t, 6),
+                    row_grad + r * Dmax, lr, eps);
+    }
     return nv;
 }
 
@@ -519,25 +586,23 @@ int64_t tbe_oracle_rows_update(int32_t T, int64_t B, int32_t D, int32_t dtype,
 /* Small-table histogram counts.                                         */
 
 /*
- * counts[(t*B + b)*Emax + e] = #{p in bag (t,b) : idx_p == e}, for
- * 0 <= e < E_t (out-of-range lookups and malformed bags are not counted).
- * Emax >= every E_t.  These are the forward's counts: a lookup that two
- * well-formed bags cover counts in both.
- * Returns the number of lookups counted.
+ * counts[g*Emax + e] = #{p in bag g : idx_p == e}, for 0 <= e < E_t
+ * (out-of-range lookups and malformed bags are not counted).  Emax >= every
+ * E_t.  These are the forward's counts: a lookup that two well-formed bags
+ * cover counts in both.  Returns the number of lookups counted.
  */
-int64_t tbe_oracle_histogram(int32_t T, int64_t B, int32_t Emax, const int64_t *table_offset,
-                             const int64_t *indices, const int64_t *offsets, int64_t N,
-                             int32_t *counts)
+int64_t tbe_oracle_histogram(int32_t T, int64_t NB, const int64_t *layout, int32_t Emax,
+                             const int64_t *table_offset, const int64_t *indices,
+                             const int64_t *offsets, int64_t N, int32_t *counts)
 {
     int64_t total = 0;
-    memset(counts, 0, sizeof(int32_t) * (size_t)T * (size_t)B * (size_t)Emax);
-    for (int64_t g = 0; g < (int64_t)T * B; ++g) {
-        int64_t t = g / B;
-        int64_t E = table_offset[t + 1] - table_offset[t];
-        int64_t s = offsets[g], e = offsets[g + 1];
-        if (!(0 <= s && s <= e && e <= N))
+    memset(counts, 0, sizeof(int32_t) * (size_t)NB * (size_t)Emax);
+    for (int64_t g = 0; g < NB; ++g) {
+        if (!well_formed(offsets, g, N))
             continue;                    /* malformed bag: empty */
-        for (int64_t p = s; p < e; ++p) {
+        int64_t t = table_of_bag(layout, T, g);
+        int64_t E = table_offset[t + 1] - table_offset[t];
+        for (int64_t p = offsets[g]; p < offsets[g + 1]; ++p) {
             int64_t idx = indices[p];
             if (idx < 0 || idx >= E)
                 continue;

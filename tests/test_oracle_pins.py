@@ -472,3 +472,93 @@ def test_offsets_check_patterns():
     assert r[0] and r[1] >= 1 and r[2]               # decreasing
     o = base.copy(); o[-1] = N + 1
     assert chk(o) == (True, 1, False, True)          # last bag past N
+
+
+# ---------------------------------------------------------------- tables of different shapes
+
+def _mixed(vbe, weighted=False, seed=23):
+    return workloads.make_workload(
+        "mixed", T=4, table_rows=[13, 40, 7, 25], D=8, dtype="f32", B=11,
+        lengths=("poisson", 4.0), dist=("zipf", 1.1), seed=seed, oob_frac=0.04,
+        weighted=[True, False, True, True] if weighted else None,
+        table_dims=[8, 16, 4, 12], table_dtypes=["f32", "bf16", "f32", "f16"],
+        table_B=[11, 5, 17, 2] if vbe else None)
+
+
+def _single_table(wl, t, W, G):
+    """Table t of a multi-shape workload as a one-table uniform problem, with
+    its weights and upstream gradient."""
+    L = wl.layout()[t]
+    g0, g1 = L["bag_off"], L["bag_off"] + L["B"]
+    s0, s1 = int(wl.offsets[g0]), int(wl.offsets[g1])
+    one = workloads.Workload(
+        name="one", T=1, B=L["B"], D=L["D"], dtype=L["dtype"], table_rows=wl.table_rows[t:t + 1].copy(),
+        offsets=(wl.offsets[g0:g1 + 1].astype(np.int64) - s0), indices=wl.indices[s0:s1].copy(),
+        per_sample_weights=None if wl.per_sample_weights is None else wl.per_sample_weights[s0:s1].copy(),
+        weighted_tables=None if wl.weighted_tables is None else wl.weighted_tables[t:t + 1].copy(),
+        lr=wl.lr, eps=wl.eps)
+    nbytes = int(wl.table_rows[t]) * L["D"] * (4 if L["dtype"] == "f32" else 2)
+    raw = W[L["wbyte"]:L["wbyte"] + nbytes]
+    Wt = raw.view(np.float32 if L["dtype"] == "f32" else np.uint16).reshape(-1, L["D"])
+    if wl.vbe:
+        Gt = G[L["out_off"]:L["out_off"] + L["B"] * L["D"]].reshape(L["B"], L["D"])
+    else:
+        Gt = G.reshape(wl.B, -1)[:, L["out_off"]:L["out_off"] + L["D"]]
+    return one, Wt, np.ascontiguousarray(Gt)
+
+
+def _table_out(wl, out, t):
+    L = wl.layout()[t]
+    if wl.vbe:
+        return out[L["out_off"]:L["out_off"] + L["B"] * L["D"]].reshape(L["B"], L["D"])
+    return out.reshape(wl.B, -1)[:, L["out_off"]:L["out_off"] + L["D"]]
+
+
+@pytest.mark.parametrize("vbe", [False, True])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_multi_shape_tables_decompose_into_single_tables(vbe, weighted):
+    # tables are independent problems: a batch of tables with different D,
+    # dtype (and, with VBE, B) equals each table run alone in the pinned
+    # uniform oracle -- pooled rows, updated weights and momentum, bit for bit
+    wl = _mixed(vbe, weighted)
+    W = wl.weights_mixed()
+    G = wl.grad_out()
+    m0 = np.random.default_rng(3).uniform(0, 1, wl.rows_total).astype(np.float32)
+    out, _, oob, _ = oracle.forward(wl, W)
+    Wn, m, U, _, _ = oracle.backward_adagrad(wl, W, m0, G)
+    to = wl.table_offset
+    oob_sum = U_sum = 0
+    for t in range(wl.T):
+        one, Wt, Gt = _single_table(wl, t, W, G)
+        o1, _, k1, _ = oracle.forward(one, Wt)
+        np.testing.assert_array_equal(_table_out(wl, out, t), o1)
+        W1, m1, U1, _, _ = oracle.backward_adagrad(one, Wt, m0[to[t]:to[t + 1]], Gt)
+        _, Wnt, _ = _single_table(wl, t, Wn, G)
+        np.testing.assert_array_equal(Wnt, W1)
+        np.testing.assert_array_equal(m[to[t]:to[t + 1]], m1)
+        oob_sum += k1
+        U_sum += U1
+    assert oob == oob_sum > 0 and U == U_sum
+
+
+def test_vbe_forward_equals_dense_onehot_per_table():
+    wl = _mixed(True, weighted=True, seed=29)
+    W = wl.weights_mixed()
+    out, _, _, _ = oracle.forward(wl, W)
+    for t, L in enumerate(wl.layout()):
+        E = int(wl.table_rows[t])
+        A = np.zeros((L["B"], E))
+        for b in range(L["B"]):
+            g = L["bag_off"] + b
+            for p in range(wl.offsets[g], wl.offsets[g + 1]):
+                e = int(wl.indices[p])
+                if 0 <= e < E:
+                    A[b, e] += float(wl.per_sample_weights[p]) if wl.weighted_tables[t] else 1.0
+        nbytes = E * L["D"] * (4 if L["dtype"] == "f32" else 2)
+        raw = W[L["wbyte"]:L["wbyte"] + nbytes]
+        if L["dtype"] == "f32":
+            Wt = raw.view(np.float32).reshape(E, L["D"]).astype(np.float64)
+        else:
+            tdt = torch.float16 if L["dtype"] == "f16" else torch.bfloat16
+            Wt = torch.from_numpy(raw.view(np.int16).copy()).view(tdt).to(torch.float64).numpy().reshape(E, L["D"])
+        np.testing.assert_allclose(_table_out(wl, out, t), A @ Wt, rtol=1e-6, atol=1e-9)

@@ -46,14 +46,86 @@ class Workload:
     w_init: float = 0.01
     seed: int = 0
     desc: str = ""
+    # Tables of different shapes in one batch (None: every table has D,
+    # dtype and B above).  table_dims / table_dtypes give each table its own
+    # row length and weight type; table_B its own number of bags (variable
+    # batch size per table).
+    table_dims: Optional[np.ndarray] = None
+    table_dtypes: Optional[Sequence[str]] = None
+    table_B: Optional[np.ndarray] = None
 
     @property
     def N(self) -> int:
         return int(self.indices.shape[0])
 
     @property
+    def mixed(self) -> bool:
+        return self.table_dims is not None or self.table_dtypes is not None or self.table_B is not None
+
+    @property
+    def vbe(self) -> bool:
+        return self.table_B is not None
+
+    def Dt(self, t: int) -> int:
+        return int(self.table_dims[t]) if self.table_dims is not None else self.D
+
+    def dtype_t(self, t: int) -> str:
+        return self.table_dtypes[t] if self.table_dtypes is not None else self.dtype
+
+    def Bt(self, t: int) -> int:
+        return int(self.table_B[t]) if self.table_B is not None else self.B
+
+    @property
     def NB(self) -> int:
-        return self.T * self.B
+        return int(sum(self.Bt(t) for t in range(self.T)))
+
+    @property
+    def Dmax(self) -> int:
+        return max(self.Dt(t) for t in range(self.T))
+
+    def layout(self) -> list:
+        """Where each table's data lives: per table a dict of
+          wbyte    first byte of its rows in the weight buffer (16-byte aligned)
+          out_off  index in out / grad_out of its bag 0's first element
+          stride   elements from one bag's row to the next in out / grad_out
+          bag_off  CSR bag index of its bag 0
+          B, D, dtype
+        Without VBE, bag rows are rows of a [B, sum D_t] matrix (table t at
+        columns sum_{t'<t} D_t'); with VBE, each table's bag rows are packed
+        one after another, table after table."""
+        lay, wb, bag, col, voff = [], 0, 0, 0, 0
+        width = sum(self.Dt(t) for t in range(self.T))
+        for t in range(self.T):
+            D, dt, B = self.Dt(t), self.dtype_t(t), self.Bt(t)
+            if self.vbe:
+                out_off, stride = voff, D
+                voff += B * D
+            else:
+                out_off, stride = col, width
+                col += D
+            lay.append(dict(wbyte=wb, out_off=out_off, stride=stride, bag_off=bag, B=B, D=D, dtype=dt))
+            wb += self._table_bytes(t)
+            bag += B
+        return lay
+
+    def _table_bytes(self, t: int) -> int:
+        # one [rows_total, D] array when every table has the same D and dtype;
+        # tables of different shapes each start on a 16-byte boundary
+        nbytes = int(self.table_rows[t]) * self.Dt(t) * DTYPE_BYTES[self.dtype_t(t)]
+        if self.table_dims is None and self.table_dtypes is None:
+            return nbytes
+        return (nbytes + 15) // 16 * 16
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.layout()[-1]["wbyte"] + self._table_bytes(self.T - 1)
+
+    @property
+    def out_size(self) -> int:
+        """Elements of out / grad_out."""
+        if self.vbe:
+            return int(sum(self.Bt(t) * self.Dt(t) for t in range(self.T)))
+        return self.B * int(sum(self.Dt(t) for t in range(self.T)))
 
     @property
     def table_offset(self) -> np.ndarray:
@@ -89,9 +161,30 @@ class Workload:
         w.uniform_(-self.w_init, self.w_init, generator=g)
         return w
 
+    def weights_mixed(self) -> np.ndarray:
+        """Initial weights of tables of different shapes: one byte buffer laid
+        out as layout() says, each table's rows ~ U(-w_init, w_init) in its
+        own dtype (float32 rounded to it by torch)."""
+        import torch
+        rng = np.random.default_rng(self.seed + 101)
+        buf = np.zeros(self.weight_bytes, np.uint8)
+        for t, L in enumerate(self.layout()):
+            v = rng.uniform(-self.w_init, self.w_init,
+                            size=(int(self.table_rows[t]), L["D"])).astype(np.float32)
+            if L["dtype"] == "f32":
+                raw = v.view(np.uint8).reshape(-1)
+            else:
+                tdt = torch.float16 if L["dtype"] == "f16" else torch.bfloat16
+                raw = torch.from_numpy(v).to(tdt).view(torch.int16).numpy().view(np.uint8).reshape(-1)
+            buf[L["wbyte"]:L["wbyte"] + raw.size] = raw
+        return buf
+
     def grad_out(self) -> np.ndarray:
-        """Upstream gradient of the pooled output, float32 [B, T*D] ~ N(0, 1)."""
+        """Upstream gradient of the pooled output ~ N(0, 1): float32 [B, T*D]
+        (flat [out_size] for tables of different shapes)."""
         rng = np.random.default_rng(self.seed + 202)
+        if self.mixed:
+            return rng.standard_normal(size=self.out_size, dtype=np.float32)
         return rng.standard_normal(size=(self.B, self.T * self.D), dtype=np.float32)
 
     def momentum(self) -> np.ndarray:
@@ -153,7 +246,9 @@ def make_workload(name: str, T: int, table_rows: Sequence[int], D: int, dtype: s
                   B: int, lengths: tuple, dist, seed: int = 0,
                   weighted: Optional[Sequence[bool]] = None, lr: float = 0.01,
                   eps: float = 1e-8, w_init: float = 0.01, oob_frac: float = 0.0,
-                  desc: str = "") -> Workload:
+                  desc: str = "", table_dims: Optional[Sequence[int]] = None,
+                  table_dtypes: Optional[Sequence[str]] = None,
+                  table_B: Optional[Sequence[int]] = None) -> Workload:
     """Draw one workload.
 
     ``dist`` is one tuple for all tables or a list of T tuples.  ``weighted``
@@ -167,23 +262,25 @@ def make_workload(name: str, T: int, table_rows: Sequence[int], D: int, dtype: s
     assert table_rows.shape == (T,)
     dists = list(dist) if isinstance(dist, list) else [dist] * T
     rng = np.random.default_rng(seed)
-    lens = np.stack([_draw_lengths(rng, B, lengths) for _ in range(T)])   # [T, B]
-    offsets = np.zeros(T * B + 1, dtype=np.int64)
-    np.cumsum(lens.reshape(-1), out=offsets[1:])
+    Bt = [int(x) for x in table_B] if table_B is not None else [B] * T
+    lens = np.concatenate([_draw_lengths(rng, Bt[t], lengths) for t in range(T)])
+    bag0 = np.concatenate([[0], np.cumsum(Bt)])          # first bag of each table
+    offsets = np.zeros(int(bag0[-1]) + 1, dtype=np.int64)
+    np.cumsum(lens, out=offsets[1:])
     N = int(offsets[-1])
     if N >= 2**31:
         raise ValueError("workload needs more than 2^31 lookups")
     indices = np.empty(N, dtype=np.int32)
     cdf_cache: dict = {}
     for t in range(T):
-        a, b = int(offsets[t * B]), int(offsets[(t + 1) * B])
+        a, b = int(offsets[bag0[t]]), int(offsets[bag0[t + 1]])
         indices[a:b] = _draw_rows(rng, int(table_rows[t]), b - a, dists[t], cdf_cache)
     if oob_frac > 0 and N > 0:
         k = max(1, int(N * oob_frac))
         where = rng.choice(N, size=k, replace=False)
         bad = rng.integers(0, 2, size=k)
-        tab = np.searchsorted(offsets, where, side="right") - 1
-        tab = tab // B
+        bag = np.searchsorted(offsets, where, side="right") - 1
+        tab = np.searchsorted(bag0, bag, side="right") - 1
         big = table_rows[tab] + rng.integers(0, 1000, size=k)
         indices[where] = np.where(bad == 0, -1 - rng.integers(0, 1000, size=k), big).astype(np.int32)
     psw = wt = None
@@ -193,7 +290,10 @@ def make_workload(name: str, T: int, table_rows: Sequence[int], D: int, dtype: s
     return Workload(name=name, T=T, B=B, D=D, dtype=dtype, table_rows=table_rows,
                     offsets=offsets.astype(np.int32), indices=indices,
                     per_sample_weights=psw, weighted_tables=wt, lr=lr, eps=eps,
-                    w_init=w_init, seed=seed, desc=desc)
+                    w_init=w_init, seed=seed, desc=desc,
+                    table_dims=None if table_dims is None else np.asarray(table_dims, np.int64),
+                    table_dtypes=None if table_dtypes is None else list(table_dtypes),
+                    table_B=None if table_B is None else np.asarray(table_B, np.int64))
 
 
 # --------------------------------------------------------------------------
