@@ -131,15 +131,48 @@ typedef struct tbe_config {
     int32_t key_bytes;
 } tbe_config;
 
-/* The tables: all T tables stored back to back in one [rows_total, D] array. */
+/* Shape of one table when tables differ (TorchEasyRec analysis, section 1:
+ * one fused lookup for all features of a KeyedJagged batch, whose embedding
+ * sizes differ). */
+typedef struct tbe_table_layout {
+    int64_t weights_byte_offset;        /* first byte of the table's rows in `weights`;
+                                           16-byte aligned, tables' regions disjoint */
+    int32_t D;                          /* elements per row */
+    int32_t dtype;                      /* tbe_dtype of its rows */
+} tbe_table_layout;
+
+/* The tables.  Uniform (layout == NULL): all T tables back to back in one
+ * [rows_total, D] array of dtype.  Otherwise table t holds E_t rows of
+ * layout[t].D elements of layout[t].dtype at byte layout[t].weights_byte_offset
+ * of `weights`; D and dtype are then ignored.  Either way table t owns the
+ * linearised rows [table_offset[t], table_offset[t+1]) (the keys of the batch
+ * inversion and the indices of the momentum array). */
 typedef struct tbe_tables {
-    void *weights;                      /* device, [rows_total, D] of dtype, 16-byte aligned */
+    void *weights;                      /* device, 16-byte aligned */
     const int64_t *table_offset;        /* device, [T+1]: table t owns rows [off[t], off[t+1]) */
     const int64_t *table_offset_host;   /* host copy of the same [T+1] values */
     int32_t T;
     int32_t D;
     int32_t dtype;                      /* tbe_dtype */
+    const tbe_table_layout *layout;     /* device [T] or NULL (uniform) */
+    const tbe_table_layout *layout_host;/* host copy of the same [T] records */
 } tbe_tables;
+
+/* Where one table's bags and their output rows lie in a batch: its bags are
+ * CSR bags bag_offset .. bag_offset + B - 1 (tables follow one another,
+ * bag_offset[0] = 0), and bag b's pooled row (D_t floats) starts at
+ * out[out_offset + b * out_stride]; grad_out has the same layout.  Variable
+ * batch size per table (VBE, FBTriton TBE redesign, decision checklist item
+ * 5) is a different B per table, its rows packed one after another
+ * (out_offset = sum of earlier tables' B*D, out_stride = D); tables of
+ * different D with one B use out_offset = sum of earlier tables' D and
+ * out_stride = the sum of all D (rows of a [B, sum D] matrix). */
+typedef struct tbe_bag_layout {
+    int64_t bag_offset;
+    int64_t B;
+    int64_t out_offset;                 /* multiple of 4 */
+    int64_t out_stride;                 /* multiple of 4 */
+} tbe_bag_layout;
 
 /* Element type of a batch's indices and offsets (decision checklist item 6:
  * int32 where the range allows, int64 otherwise; KeyedJagged tensors often
@@ -157,6 +190,12 @@ typedef struct tbe_batch {
     const uint8_t *weighted_tables;     /* device, [T] or NULL: nonzero = table uses the weights;
                                            NULL with weights given = every table weighted */
     int32_t index_type;                 /* tbe_index_type of indices and offsets */
+    /* NULL: every table has B bags, bag (t,b) is CSR bag t*B+b and its row is
+     * out[b, t*D .. t*D+D) of a [B, T*D] out.  Required when the tables have
+     * a layout; B is then ignored. */
+    const tbe_bag_layout *bag_layout;      /* device [T] or NULL */
+    const tbe_bag_layout *bag_layout_host; /* host copy */
+    int64_t out_size;                   /* with bag_layout: floats in out and in grad_out */
 } tbe_batch;
 
 /*

@@ -92,19 +92,17 @@ class _Problem:
 
 
 def _wbytes(W: np.ndarray, wl) -> np.ndarray:
-    """Weights as raw storage bytes: a float32 array for f32 tables, uint16 bit
-    patterns for f16/bf16 tables, or the byte buffer of tables of different
-    shapes."""
-    if not wl.mixed:
-        if wl.dtype == "f32":
-            W = np.ascontiguousarray(W, dtype=np.float32)
-        else:
-            assert W.dtype == np.uint16, "f16/bf16 weights are passed as uint16 bit patterns"
-            W = np.ascontiguousarray(W)
-    else:
-        assert W.dtype == np.uint8, "tables of different shapes pass their weights as bytes"
-        W = np.ascontiguousarray(W)
-    return W
+    """Weights as raw storage: a float32 array for f32 tables, uint16 bit
+    patterns for f16/bf16 tables, or a byte buffer laid out as wl.layout()
+    says (required for tables of different D or dtype)."""
+    if W.dtype == np.uint8:
+        return np.ascontiguousarray(W)
+    assert wl.table_dims is None and wl.table_dtypes is None, \
+        "tables of different shapes pass their weights as bytes"
+    if wl.dtype == "f32":
+        return np.ascontiguousarray(W, dtype=np.float32)
+    assert W.dtype == np.uint16, "f16/bf16 weights are passed as uint16 bit patterns"
+    return np.ascontiguousarray(W)
 
 
 def forward(wl, W: np.ndarray, bags: Optional[np.ndarray] = None, want_abs: bool = False):

@@ -41,6 +41,10 @@ struct BwdParams {
     float *mom;
     const float *G;
     const int64_t *table_offset;
+    const tbe_table_layout *layout;     // nullable: uniform tables
+    const tbe_bag_layout *bag_layout;   // nullable: uniform bags and gradient rows
+    int cls_dtype;                      // with a layout: this launch's class (D is p.D)
+    int64_t part_stride;                // bytes from one chunk slot's partial to the next
     const uint32_t *vals;
     const int32_t *bag_of;
     const float *psw;
@@ -70,6 +74,24 @@ struct BwdParams {
 __device__ __forceinline__ int64_t load_key(const BwdParams &p, int64_t r) {
     return p.key64 ? (int64_t)__ldg(reinterpret_cast<const unsigned long long *>(p.unique_keys) + r)
                    : (int64_t)__ldg(reinterpret_cast<const uint32_t *>(p.unique_keys) + r);
+}
+
+// weight row of linearised row `key` of table t (row length p.D)
+template <typename WT> __device__ __forceinline__ WT *wrow_of(const BwdParams &p, int t, int64_t key) {
+    return reinterpret_cast<WT *>(reinterpret_cast<char *>(p.W) +
+                                  weight_byte(p.layout, p.table_offset, t, key, p.D, (int)sizeof(WT)));
+}
+
+// bag within table t of a sorted payload: the bag itself (unweighted
+// batches) or, for a lookup position, its CSR bag less the table's first
+__device__ __forceinline__ int64_t payload_bag(const BwdParams &p, uint32_t v, int t) {
+    if (!p.payload_pos) return (int64_t)v;
+    return (int64_t)__ldg(p.bag_of + v) - bag_base(p.bag_layout, p.B, t);
+}
+
+// bags of table t
+__device__ __forceinline__ int64_t bags_of(const BwdParams &p, int t) {
+    return p.bag_layout == nullptr ? p.B : __ldg(&p.bag_layout[t].B);
 }
 
 __device__ __forceinline__ void acc4(double (&a)[4], const float4 x, float w) {
@@ -146,9 +168,14 @@ __device__ __forceinline__ void ld_part(float (&a)[4], const float *p) {
 
 // acc += partials of chunk slots cb .. cb+nch-1, added strictly in chunk
 // order; PB slots are loaded ahead so that many loads are in flight.
+// partial of chunk slot `slot` (stride bytes apart)
+template <typename ACC> __device__ __forceinline__ ACC *part_of(void *partials, int64_t stride, int64_t slot) {
+    return reinterpret_cast<ACC *>(reinterpret_cast<char *>(partials) + slot * stride);
+}
+
 template <bool L2ONLY, typename ACC, int LPR, int NV>
-__device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], const ACC *part, int cb, int nch,
-                                             int D, int li) {
+__device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], void *partials, int64_t stride, int cb,
+                                             int nch, int li) {
     constexpr int PB = NV >= 2 ? 2 : 4;
     for (int c0 = 0; c0 < nch; c0 += PB) {
         ACC v[PB][NV][4];
@@ -157,7 +184,7 @@ __device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], const ACC *part,
             if (c0 + j < nch)
 #pragma unroll
                 for (int q = 0; q < NV; ++q)
-                    ld_part<L2ONLY>(v[j][q], part + (int64_t)(cb + c0 + j) * D + li * 4 + q * LPR * 4);
+                    ld_part<L2ONLY>(v[j][q], part_of<ACC>(partials, stride, cb + c0 + j) + li * 4 + q * LPR * 4);
 #pragma unroll
         for (int j = 0; j < PB; ++j)
             if (c0 + j < nch)
@@ -217,6 +244,7 @@ struct Chunk {
     int64_t key;
     int t, l, cb, nch; // table, long run, its first chunk slot and chunk count
     int slot;          // chunk slot (index of its descriptor and its partial)
+    bool skip;         // a table of another launch's class: nothing to do here
 };
 
 // the chunk taken ci-th: slot chunk_order[ci], or ci without an order
@@ -230,6 +258,8 @@ __device__ __forceinline__ Chunk load_chunk(const BwdParams &p, int ci) {
     c.t = table_of_key(p.table_offset, p.T, c.key);
     c.l = b.x; c.cb = b.y; c.nch = b.z;
     c.slot = slot;
+    c.skip = !in_class(p.layout, c.t, p.D, p.cls_dtype);
+    if (c.skip) c.e = c.s;
     return c;
 }
 // Exact rowwise Adagrad arithmetic, m += mean_d(g^2); w -= lr*g/(sqrt(m)+eps),
@@ -270,7 +300,7 @@ template <> struct Adagrad<float> {
 // lanes of sub-group 0 hold meaningful values; every lane takes part in the
 // shuffles.
 template <typename WT, typename ACC, int LPR, int NV>
-__device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const BwdParams &p,
+__device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const BwdParams &p, int t,
                                               int64_t row, int lane, int sub, int li) {
     using A = Adagrad<ACC>;
     ACC ss = ACC(0);
@@ -283,7 +313,7 @@ __device__ __forceinline__ void adagrad_apply(const ACC (&acc)[NV][4], const Bwd
     if (sub != 0) return;
     const float m_new = A::mom(p.mom[row], ss, p.D);
     const auto den = A::den(m_new, p.eps);
-    WT *wr = reinterpret_cast<WT *>(p.W) + row * p.D + li * 4;
+    WT *wr = wrow_of<WT>(p, t, row) + li * 4;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
         float w[4];
@@ -347,7 +377,9 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
             e = __ldg(p.seg_off + r + 1);
             key = load_key(p, r);
         }
-        const bool mine = r < U_runs && e - s < p.sl_threshold;
+        bool mine = r < U_runs && e - s < p.sl_threshold;
+        const int t = mine ? table_of_key(p.table_offset, p.T, key) : 0;
+        mine = mine && in_class(p.layout, t, p.D, p.cls_dtype);
         ACC acc[NV][4];
 #pragma unroll
         for (int q = 0; q < NV; ++q)
@@ -355,17 +387,19 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
         typename WRaw<WT>::t wraw[NV];
         float m_old = 0.f;
-        WT *wr = reinterpret_cast<WT *>(p.W) + key * p.D;
+        WT *wr = mine ? wrow_of<WT>(p, t, key) : nullptr;
         if (mine) {
 #pragma unroll
             for (int q = 0; q < NV; ++q) wraw[q] = ld_wraw(wr + (gl + q * GL) * 4);
             m_old = p.mom[key];
-            const int t = table_of_key(p.table_offset, p.T, key);
             const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
-            const float *Gt = p.G + (int64_t)t * p.D + gl * 4;
-            const int64_t tB = (int64_t)t * p.B;
+            // gradient row of bag b: G + g0 + b * gs
+            const float *Gt = p.G + (p.bag_layout ? __ldg(&p.bag_layout[t].out_offset) : (int64_t)t * p.D) +
+                              gl * 4;
+            const int64_t gs = p.bag_layout ? __ldg(&p.bag_layout[t].out_stride) : TD;
+            const int64_t Bt = bags_of(p, t);
             for (int32_t i = s; i < e; i += U) {
-                int bk[U];
+                int64_t bk[U];
                 float wk[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -373,16 +407,11 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
                     wk[u] = 1.f;
                     if (i + u < e) {
                         const uint32_t v = __ldg(p.vals + i + u);
-                        int b;
-                        if (p.payload_pos) {
-                            b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
-                            if (wt) wk[u] = __ldg(p.psw + v);
-                        } else {
-                            b = (int)v;
-                        }
+                        const int64_t b = payload_bag(p, v, t);
+                        if (p.payload_pos && wt) wk[u] = __ldg(p.psw + v);
                         // only malformed (overlapping) offsets can give a bag
                         // outside the run's table; such a lookup adds nothing
-                        bk[u] = (b >= 0 && (int64_t)b < p.B) ? b : -1;
+                        bk[u] = (b >= 0 && b < Bt) ? b : -1;
                     }
                 }
                 float4 x[U][NV];
@@ -391,8 +420,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
                     if (bk[u] >= 0)
 #pragma unroll
                         for (int q = 0; q < NV; ++q)
-                            x[u][q] = __ldg(reinterpret_cast<const float4 *>(
-                                Gt + (int64_t)bk[u] * TD + q * GL * 4));
+                            x[u][q] = __ldg(reinterpret_cast<const float4 *>(Gt + bk[u] * gs + q * GL * 4));
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     if (bk[u] >= 0)
@@ -458,7 +486,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 
     const uint32_t row_bytes = (uint32_t)p.D * 4;
     const int R = STAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
-    const int64_t rowstride = (int64_t)p.T * p.D;
+    const float4 *G4 = reinterpret_cast<const float4 *>(p.G);
 
     // payload of lookups [s, s + PV*32) into registers (issued early)
     uint32_t pv[PV];
@@ -469,26 +497,23 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             pv[k] = i < c.e ? __ldg(p.vals + i) : 0u;
         }
     };
-    // offset from G_t (in 16-byte vectors) and weight of each lookup of c into buffer buf
+    // offset from G (in 16-byte vectors) of each lookup's gradient row and its
+    // weight, for the lookups of c, into buffer buf
     auto stage = [&](const Chunk &c, int buf) {
         const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + c.t) != 0);
-        const int64_t tB = (int64_t)c.t * p.B;
         const int n = c.e - c.s;
+        const int64_t g0 = p.bag_layout ? __ldg(&p.bag_layout[c.t].out_offset) : (int64_t)c.t * p.D;
+        const int64_t gs = p.bag_layout ? __ldg(&p.bag_layout[c.t].out_stride) : (int64_t)p.T * p.D;
+        const int64_t Bt = bags_of(p, c.t);
         uint32_t *o = offb + buf * p.chunk;
         float *w = wgt + buf * p.chunk;
         auto put = [&](int i, uint32_t v) {
-            int b;
-            float x = 1.f;
-            if (p.payload_pos) {
-                b = (int)((int64_t)__ldg(p.bag_of + v) - tB);
-                if (wt) x = __ldg(p.psw + v);
-            } else {
-                b = (int)v;
-            }
+            const int64_t b = payload_bag(p, v, c.t);
+            const float x = p.payload_pos && wt ? __ldg(p.psw + v) : 1.f;
             // only malformed (overlapping) offsets can give a bag outside the
             // run's table: such a lookup copies row 0 with weight 0
-            const bool ok = b >= 0 && (int64_t)b < p.B;
-            o[i] = ok ? (uint32_t)(((int64_t)b * rowstride) >> 2) : 0u;   // 16-byte units
+            const bool ok = b >= 0 && b < Bt;
+            o[i] = ok ? (uint32_t)((g0 + b * gs) >> 2) : 0u;   // 16-byte units
             w[i] = ok ? x : 0.f;
         };
 #pragma unroll
@@ -505,10 +530,9 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         const uint32_t bar = bar0 + 8 * st;
         if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
         __syncwarp();
-        const float4 *Gt = reinterpret_cast<const float4 *>(p.G + (int64_t)c.t * p.D);
         const uint32_t *o = offb + buf * p.chunk + k * R;
         const uint32_t dst0 = ring0 + st * STAGE_BYTES;
-        for (int j = lane; j < rows; j += 32) bulk_g2s(dst0 + j * row_bytes, Gt + o[j], row_bytes, bar);
+        for (int j = lane; j < rows; j += 32) bulk_g2s(dst0 + j * row_bytes, G4 + o[j], row_bytes, bar);
         ++gprod;
     };
 
@@ -585,11 +609,11 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             for (int q = 0; q < NV; ++q)
 #pragma unroll
                 for (int x = 0; x < 4; ++x) acc[q][x] += __shfl_xor_sync(FULL, acc[q][x], sh);
-        ACC *part = reinterpret_cast<ACC *>(p.partials) + (int64_t)cur.slot * p.D + li * 4;
-        if (sub == 0)
+        ACC *part = part_of<ACC>(p.partials, p.part_stride, cur.slot) + li * 4;
+        if (sub == 0 && !cur.skip)
 #pragma unroll
             for (int q = 0; q < NV; ++q) st_part(part + q * LPR * 4, acc[q]);
-        if constexpr (FUSED) {
+        if (FUSED && !cur.skip) {
             __threadfence();
             __syncwarp();
             int old = 0;
@@ -602,9 +626,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 #pragma unroll
                     for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
                 if (sub == 0)
-                    sum_partials<true, ACC, LPR, NV>(acc, reinterpret_cast<const ACC *>(p.partials),
-                                                    cur.cb, cur.nch, p.D, li);
-                adagrad_apply<WT, ACC, LPR, NV>(acc, p, (int64_t)cur.key, lane, sub, li);
+                    sum_partials<true, ACC, LPR, NV>(acc, p.partials, p.part_stride, cur.cb, cur.nch, li);
+                adagrad_apply<WT, ACC, LPR, NV>(acc, p, cur.t, cur.key, lane, sub, li);
                 if (lane == 0) p.arrive[cur.l] = 0;
             }
         }
@@ -723,7 +746,9 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
     // weight rows of the short runs are copied into weight buffer wb
     uint32_t wphase = 0;   // bit k: parity of weight buffer k's next completion
     auto task_prepare = [&](SsTask &T, int wb) {
-        const bool mine = T.q >= 0 && lane < T.nr && T.e - T.s < p.sl_threshold;
+        bool mine = T.q >= 0 && lane < T.nr && T.e - T.s < p.sl_threshold;
+        const int tt = mine ? table_of_key(p.table_offset, p.T, T.key) : 0;
+        mine = mine && in_class(p.layout, tt, p.D, p.cls_dtype);
         T.len = mine ? T.e - T.s : 0;
         int x = T.len;
 #pragma unroll
@@ -733,7 +758,7 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
         }
         T.total = __shfl_sync(FULL, x, 31);
         T.pre = x - T.len;
-        T.t = mine ? table_of_key(p.table_offset, p.T, T.key) : 0;
+        T.t = mine ? tt : 0;
         T.mom = mine ? p.mom[T.key] : 0.f;
         const unsigned m = __ballot_sync(FULL, mine);
         if (m) {
@@ -741,8 +766,8 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
             if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)__popc(m) * (uint32_t)wrow);
             __syncwarp();
             if (mine)
-                bulk_g2s(smem_addr(wbuf + wb * SS_WBUF + lane * wrow),
-                         reinterpret_cast<const WT *>(p.W) + (int64_t)T.key * p.D, (uint32_t)wrow, bar);
+                bulk_g2s(smem_addr(wbuf + wb * SS_WBUF + lane * wrow), wrow_of<WT>(p, T.t, T.key),
+                         (uint32_t)wrow, bar);
         }
     };
     // table of block blk of task T (its lookups blk*32 + lane) into buffer tb
@@ -763,19 +788,17 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
         const int t_sl = __shfl_sync(FULL, T.t, slot);
         if (k < T.total) {
             const uint32_t v = __ldg(p.vals + s_sl + (k - pre_sl));
-            int b;
+            const int64_t b = payload_bag(p, v, t_sl);
             float x = 1.f;
-            if (p.payload_pos) {
-                b = (int)((int64_t)__ldg(p.bag_of + v) - (int64_t)t_sl * p.B);
-                if (p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t_sl) != 0))
-                    x = __ldg(p.psw + v);
-            } else {
-                b = (int)v;
-            }
+            if (p.payload_pos && p.psw != nullptr &&
+                (p.weighted == nullptr || __ldg(p.weighted + t_sl) != 0))
+                x = __ldg(p.psw + v);
             // only malformed (overlapping) offsets can give a bag outside the
             // run's table: such a lookup copies row 0 with weight 0
-            const bool ok = b >= 0 && (int64_t)b < p.B;
-            tab_off[tb * SS_BLK + lane] = ok ? (uint32_t)(((int64_t)b * TD + (int64_t)t_sl * p.D) >> 2) : 0u;
+            const bool ok = b >= 0 && b < bags_of(p, t_sl);
+            const int64_t g0 = p.bag_layout ? __ldg(&p.bag_layout[t_sl].out_offset) : (int64_t)t_sl * p.D;
+            const int64_t gs = p.bag_layout ? __ldg(&p.bag_layout[t_sl].out_stride) : TD;
+            tab_off[tb * SS_BLK + lane] = ok ? (uint32_t)((g0 + b * gs) >> 2) : 0u;
             tab_w[tb * SS_BLK + lane] = ok ? x : 0.f;
             tab_tag[tb * SS_BLK + lane] = (uint32_t)slot | (k == pre_sl + len_sl - 1 ? SS_LAST : 0u);
         }
@@ -913,10 +936,11 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
                 for (int sh = 1; sh < 32; sh <<= 1) ss += __shfl_xor_sync(FULL, ss, sh);
                 const float m_old = __shfl_sync(FULL, cur.mom, slot);
                 const int64_t key = __shfl_sync(FULL, cur.key, slot);
+                const int tk = __shfl_sync(FULL, cur.t, slot);
                 const float m_new = A::mom(m_old, ss, p.D);
                 const auto den = A::den(m_new, p.eps);
                 const WT *wsrc = reinterpret_cast<const WT *>(wbuf + cw * SS_WBUF + slot * wrow) + lane * 4;
-                WT *wdst = reinterpret_cast<WT *>(p.W) + (int64_t)key * p.D + lane * 4;
+                WT *wdst = wrow_of<WT>(p, tk, key) + lane * 4;
 #pragma unroll
                 for (int q = 0; q < NV; ++q) {
                     float w[4];
@@ -967,15 +991,15 @@ __global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
         const int32_t rs = __ldg(p.seg_off + r), re = __ldg(p.seg_off + r + 1);
         const int nch = (re - rs + p.chunk - 1) / p.chunk;
         const int64_t key = load_key(p, r);
+        const int t = table_of_key(p.table_offset, p.T, key);
+        if (!in_class(p.layout, t, p.D, p.cls_dtype)) continue;   // warp-uniform
         ACC acc[NV][4];
 #pragma unroll
         for (int q = 0; q < NV; ++q)
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
-        if (sub == 0)
-            sum_partials<false, ACC, LPR, NV>(acc, reinterpret_cast<const ACC *>(p.partials), cb,
-                                              nch, p.D, li);
-        adagrad_apply<WT, ACC, LPR, NV>(acc, p, key, lane, sub, li);
+        if (sub == 0) sum_partials<false, ACC, LPR, NV>(acc, p.partials, p.part_stride, cb, nch, li);
+        adagrad_apply<WT, ACC, LPR, NV>(acc, p, t, key, lane, sub, li);
     }
 }
 
@@ -1097,16 +1121,26 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.sl_threshold = a.sl_threshold;
     p.chunk = a.chunk;
     p.payload_pos = m->payload_is_pos;
+    p.layout = a.tab->layout;
+    p.bag_layout = a.bt->bag_layout;
+    p.part_stride = a.part_stride;
     if (a.bt->N == 0) return TBE_OK;
-    const RowPlan rp = row_plan(a.tab->D, 4);
-    bool ok = false;
-    switch (a.tab->dtype) {
-    case TBE_F32: ok = bwd_dispatch<float>(L, p, rp, a.long_mode); break;
-    case TBE_F16: ok = bwd_dispatch<__half>(L, p, rp, a.long_mode); break;
-    case TBE_BF16: ok = bwd_dispatch<__nv_bfloat16>(L, p, rp, a.long_mode); break;
-    default: return TBE_ERR_UNSUPPORTED_DTYPE;
+    // one set of launches per (D, dtype) class; with layouts each kernel
+    // skips the runs and chunks of other classes' tables
+    for (const TableClass &c : a.classes->classes) {
+        p.D = c.D;
+        p.cls_dtype = c.dtype;
+        const RowPlan rp = row_plan(c.D, 4);
+        bool ok = false;
+        switch (c.dtype) {
+        case TBE_F32: ok = bwd_dispatch<float>(L, p, rp, a.long_mode); break;
+        case TBE_F16: ok = bwd_dispatch<__half>(L, p, rp, a.long_mode); break;
+        case TBE_BF16: ok = bwd_dispatch<__nv_bfloat16>(L, p, rp, a.long_mode); break;
+        default: return TBE_ERR_UNSUPPORTED_DTYPE;
+        }
+        if (!ok) return TBE_ERR_UNSUPPORTED_DIM;
     }
-    return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
+    return TBE_OK;
 }
 
 // ---------------------------------------------------------------------------

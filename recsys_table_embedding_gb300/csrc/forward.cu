@@ -19,15 +19,27 @@
 // int64 (kernels templated on the index type IdxT); keys are written here
 // only when they are 32-bit, the 64-bit keys of row ranges of 2^31 and more
 // come from the linearize kernel.
+#include <string.h>
+
+#include <algorithm>
 #include <type_traits>
 
 #include "tbe_internal.cuh"
 
 namespace tbe {
 
+// Tables of one launch: with layouts, a launch serves the tables of one
+// (D, dtype) class, at most FWD_TLIST per launch.
+constexpr int FWD_TLIST = 256;
+
 struct FwdParams {
     const void *W;
     const int64_t *table_offset;
+    const tbe_table_layout *layout;     // nullable: uniform tables
+    const tbe_bag_layout *bag_layout;   // nullable: uniform bags and output rows
+    int ntl;                            // tables of this launch (0: all, uniform bags)
+    int32_t tlist[FWD_TLIST];           // their ids
+    int64_t tcum[FWD_TLIST + 1];        // their bags, cumulative
     const void *indices;   // IdxT [N]
     const void *offsets;   // IdxT [NB+1]
     const float *psw;
@@ -140,29 +152,46 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 // block with an out-of-range index) goes one 32/LPR-row step at a time with
 // per-row checks.  (t, b) of the next bag are stepped, not divided.
 template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED, typename IdxT>
-__global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ FwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     constexpr int VEC = VB / (int)sizeof(WT);   // elements per lane vector
     constexpr int RPI = 32 / LPR;
     constexpr int STEP = RPI * U;               // rows of a full step
     const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    int t = (int)(bag / p.B);
-    int64_t b = bag - (int64_t)t * p.B;
-    const int tstep = (int)(nwarps / p.B);
-    const int64_t bstep = nwarps - (int64_t)tstep * p.B;
+    // work item k: bag k of all tables (uniform: (t, b) stepped without
+    // division), or bag k of this launch's class tables (table found in the
+    // cumulative bag counts)
+    int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nitems = p.ntl ? p.tcum[p.ntl] : p.NB;
+    int t = p.ntl ? 0 : (int)(k / p.B);
+    int64_t b = p.ntl ? 0 : k - (int64_t)t * p.B;
+    const int tstep = p.ntl ? 0 : (int)(nwarps / p.B);
+    const int64_t bstep = p.ntl ? 0 : nwarps - (int64_t)tstep * p.B;
     int oob = 0;
     check_span<IdxT>(p);
     uint32_t *keys = reinterpret_cast<uint32_t *>(p.keys);
     const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
-    for (; bag < p.NB; bag += nwarps) {
+    for (; k < nitems; k += nwarps) {
+        int64_t bag = k;
+        if (p.ntl) {
+            int lo = 0, hi = p.ntl;   // class table lo: tcum[lo] <= k < tcum[lo+1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.tcum[mid] <= k) lo = mid; else hi = mid;
+            }
+            t = p.tlist[lo];
+            b = k - p.tcum[lo];
+            bag = bag_base(p.bag_layout, p.B, t) + b;
+        }
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
         int32_t start, end;
         read_bag<IdxT>(p, bag, lane, start, end);
         const bool wt = WEIGHTED && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
-        const WT *Wt = reinterpret_cast<const WT *>(p.W) + row0 * p.D + li * VEC;
+        const WT *Wt = reinterpret_cast<const WT *>(reinterpret_cast<const char *>(p.W) +
+                                                    weight_byte(p.layout, p.table_offset, t, row0, p.D,
+                                                                (int)sizeof(WT))) + li * VEC;
         ACC acc[NV][VEC];
 #pragma unroll
         for (int q = 0; q < NV; ++q)
@@ -228,15 +257,17 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) acc[q][e] += __shfl_xor_sync(FULL, acc[q][e], s);
         if (sub == 0) {
-            float *o = p.out + (b * p.T + t) * (int64_t)p.D + li * VEC;
+            float *o = p.out + out_row(p.bag_layout, p.T, p.D, t, b) + li * VEC;
 #pragma unroll
             for (int q = 0; q < NV; ++q) store_out<VEC>(o + q * LPR * VEC, acc[q]);
         }
-        t += tstep;
-        b += bstep;
-        if (b >= p.B) {
-            b -= p.B;
-            ++t;
+        if (!p.ntl) {
+            t += tstep;
+            b += bstep;
+            if (b >= p.B) {
+                b -= p.B;
+                ++t;
+            }
         }
     }
     oob = warp_sum_i(oob);
@@ -248,7 +279,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const FwdParams p) {
 // key and payload of every lookup; out-of-range lookups get the sentinel key
 // (the forward counts them).
 template <typename IdxT, typename KeyT>
-__global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(256) tbe_linearize_kernel(const __grid_constant__ FwdParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     check_span<IdxT>(p);
@@ -256,8 +287,8 @@ __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
     const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
     for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < p.NB;
          bag += nwarps) {
-        const int t = (int)(bag / p.B);
-        const int64_t b = bag - (int64_t)t * p.B;
+        const int t = table_of_bag(p.bag_layout, p.B, p.T, bag);
+        const int64_t b = bag - bag_base(p.bag_layout, p.B, t);
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
         int32_t start, end;
@@ -281,7 +312,7 @@ __global__ void __launch_bounds__(256) tbe_linearize_kernel(const FwdParams p) {
 // before it starts, two well-formed bags can hold one lookup, and every
 // lookup gets the sentinel: such a batch has no backward update.
 template <typename IdxT, typename KeyT>
-__global__ void __launch_bounds__(256) tbe_offsets_fixup_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(256) tbe_offsets_fixup_kernel(const __grid_constant__ FwdParams p) {
     if (__ldg(p.counters + C_MALFORMED) == 0) return;
     KeyT *keys = reinterpret_cast<KeyT *>(p.keys);
     const bool decreasing = __ldg(p.counters + C_DECREASING) != 0;
@@ -361,7 +392,7 @@ static void fwd_launch(Launch &L, const FwdParams &p) {
                               : tbe_fwd_kernel<WT, VB, LPR, NV, US, true, IdxT>)
                  : (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false, IdxT>
                               : tbe_fwd_kernel<WT, VB, LPR, NV, US, false, IdxT>);
-    const int grid = grid_for(L, k, 256, p.NB);
+    const int grid = grid_for(L, k, 256, p.ntl ? p.tcum[p.ntl] : p.NB);
     L.before("tbe_fwd_gather");
     k<<<grid, 256, 0, L.stream>>>(p);
     L.after();
@@ -400,6 +431,7 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
                              uint32_t *vals, int32_t *bag_of, uint64_t sentinel, int32_t *status,
                              int32_t *counters) {
     FwdParams p;
+    memset(&p, 0, sizeof(p));
     p.W = tab->weights;
     p.table_offset = tab->table_offset;
     p.indices = bt->indices;
@@ -419,25 +451,46 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
     p.D = tab->D;
     p.sentinel = sentinel;
     p.payload_pos = bt->per_sample_weights != nullptr ? 1 : 0;
+    p.layout = tab->layout;
+    p.bag_layout = bt->bag_layout;
+    p.ntl = 0;
     return p;
 }
 
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
                           uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
-                          int32_t *status, int32_t *counters) {
+                          int32_t *status, int32_t *counters, const TableClasses &cls) {
     FwdParams p = make_params(tab, bt, out, keys, vals, bag_of, sentinel, status, counters);
     if (p.NB == 0) return TBE_OK;
-    if (!row_plan(tab->D, tab->dtype == TBE_F32 ? 4 : 2).ok) return TBE_ERR_UNSUPPORTED_DIM;
-    if (tab->dtype != TBE_F32 && tab->dtype != TBE_F16 && tab->dtype != TBE_BF16)
-        return TBE_ERR_UNSUPPORTED_DTYPE;
-    const bool ok = bt->index_type == TBE_INDEX_I64 ? fwd_dtype<int64_t>(L, p, tab->dtype, tab->D)
-                                                    : fwd_dtype<int32_t>(L, p, tab->dtype, tab->D);
-    return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
+    const bool i64 = bt->index_type == TBE_INDEX_I64;
+    if (bt->bag_layout == nullptr && tab->layout == nullptr) {   // uniform: one launch
+        const bool ok = i64 ? fwd_dtype<int64_t>(L, p, tab->dtype, tab->D)
+                            : fwd_dtype<int32_t>(L, p, tab->dtype, tab->D);
+        return ok ? TBE_OK : TBE_ERR_UNSUPPORTED_DIM;
+    }
+    // one launch per (D, dtype) class and per FWD_TLIST of its tables
+    for (const TableClass &c : cls.classes) {
+        for (size_t i0 = 0; i0 < c.tables.size(); i0 += FWD_TLIST) {
+            const size_t n = std::min(c.tables.size() - i0, (size_t)FWD_TLIST);
+            p.D = c.D;
+            p.ntl = (int)n;
+            p.tcum[0] = 0;
+            for (size_t i = 0; i < n; ++i) {
+                const int t = c.tables[i0 + i];
+                p.tlist[i] = t;
+                p.tcum[i + 1] = p.tcum[i] + cls.B[t];
+            }
+            if (p.tcum[n] == 0) continue;
+            const bool ok = i64 ? fwd_dtype<int64_t>(L, p, c.dtype, c.D) : fwd_dtype<int32_t>(L, p, c.dtype, c.D);
+            if (!ok) return TBE_ERR_UNSUPPORTED_DIM;
+        }
+    }
+    return TBE_OK;
 }
 
 template <typename IdxT, typename KeyT> static void linearize_launch(Launch &L, const FwdParams &p) {
     auto k = tbe_linearize_kernel<IdxT, KeyT>;
-    const int grid = grid_for(L, k, 256, p.NB);
+    const int grid = grid_for(L, k, 256, p.ntl ? p.tcum[p.ntl] : p.NB);
     L.before("tbe_linearize");
     k<<<grid, 256, 0, L.stream>>>(p);
     L.after();

@@ -4,10 +4,13 @@
 // stream; no device memory is allocated and no host synchronisation happens.
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <set>
 #include <tuple>
+#include <utility>
+#include <vector>
 
 #include "tbe_internal.cuh"
 
@@ -99,13 +102,80 @@ static int bits_for(int64_t v) {   // bits needed to represent v >= 0
 
 struct Problem {
     int64_t N, B, NB, rows_total, max_rows;
-    int T, D, dtype;
+    int T, D, dtype;    // with layouts: D = the largest D, dtype = TBE_F32 if any table is FP32
     int key_bits, key_bytes, index_type;
     int path;           // 1 generic, 2 histogram
     int payload_pos;
     int64_t max_long, max_chunks;
     int sl_threshold, chunk, long_mode;
+    bool layouts;       // tables or bags described by per-table layouts
+    TableClasses classes;
 };
+
+// Tables and bags described by layouts: every table's shape is supported,
+// weight regions are disjoint, bags follow one another and every output row
+// lies inside out.  Fills the launch classes, NB, and the largest D.
+static tbe_status check_layouts(const tbe_tables *tab, const tbe_batch *bt, Problem *pr) {
+    const int T = tab->T;
+    const int64_t *to = tab->table_offset_host;
+    if (tab->layout != nullptr && (tab->layout_host == nullptr || bt->bag_layout == nullptr))
+        return TBE_ERR_NULL_POINTER;
+    if (bt->bag_layout != nullptr && bt->bag_layout_host == nullptr) return TBE_ERR_NULL_POINTER;
+    if (!aligned(tab->layout, 8) || !aligned(bt->bag_layout, 8)) return TBE_ERR_MISALIGNED;
+    pr->classes.classes.clear();
+    pr->classes.B.assign(T, 0);
+    int Dmax = 0, any32 = 0;
+    // table shapes and disjoint weight regions
+    std::vector<std::pair<int64_t, int64_t>> regions;
+    for (int t = 0; t < T; ++t) {
+        const int D = tab->layout_host ? tab->layout_host[t].D : tab->D;
+        const int dt = tab->layout_host ? tab->layout_host[t].dtype : tab->dtype;
+        if (dt != TBE_F32 && dt != TBE_F16 && dt != TBE_BF16) return TBE_ERR_UNSUPPORTED_DTYPE;
+        const int esz = dt == TBE_F32 ? 4 : 2;
+        if (D < 1 || !row_plan(D, esz).ok || !row_plan(D, 4).ok) return TBE_ERR_UNSUPPORTED_DIM;
+        if (tab->layout_host) {
+            const int64_t w0 = tab->layout_host[t].weights_byte_offset;
+            if (w0 < 0 || w0 % 16) return TBE_ERR_MISALIGNED;
+            regions.push_back({w0, w0 + (to[t + 1] - to[t]) * D * esz});
+        }
+        Dmax = D > Dmax ? D : Dmax;
+        any32 |= dt == TBE_F32;
+        size_t k = 0;
+        while (k < pr->classes.classes.size() &&
+               (pr->classes.classes[k].D != D || pr->classes.classes[k].dtype != dt))
+            ++k;
+        if (k == pr->classes.classes.size()) pr->classes.classes.push_back(TableClass{D, dt, {}});
+        pr->classes.classes[k].tables.push_back(t);
+    }
+    std::sort(regions.begin(), regions.end());
+    for (size_t i = 1; i < regions.size(); ++i)
+        if (regions[i].first < regions[i - 1].second) return TBE_ERR_INVALID_ARGUMENT;
+    // bags and output rows
+    int64_t NB = 0;
+    for (int t = 0; t < T; ++t) {
+        const int D = tab->layout_host ? tab->layout_host[t].D : tab->D;
+        int64_t B = bt->B, o0 = (int64_t)t * D, os = (int64_t)T * D;
+        if (bt->bag_layout_host) {
+            const tbe_bag_layout &L = bt->bag_layout_host[t];
+            if (L.bag_offset != NB || L.B < 0) return TBE_ERR_INVALID_ARGUMENT;
+            B = L.B;
+            o0 = L.out_offset;
+            os = L.out_stride;
+            if (o0 < 0 || o0 % 4 || os % 4 || (B > 1 && os < D)) return TBE_ERR_INVALID_ARGUMENT;
+            if (B > 0 && o0 + (B - 1) * os + D > bt->out_size) return TBE_ERR_INVALID_ARGUMENT;
+        }
+        pr->classes.B[t] = B;
+        NB += B;
+    }
+    if (NB >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
+    // the backward stages gradient-row offsets as 32-bit counts of 16-byte
+    // vectors: grad_out must stay under 64 GB
+    if (bt->out_size / 4 >= (int64_t(1) << 32)) return TBE_ERR_INVALID_ARGUMENT;
+    pr->NB = NB;
+    pr->D = Dmax;
+    pr->dtype = any32 ? TBE_F32 : TBE_BF16;
+    return TBE_OK;
+}
 
 static tbe_config defaults(const tbe_config *cfg) {
     tbe_config c;
@@ -123,11 +193,14 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     if (tab == nullptr || bt == nullptr) return TBE_ERR_NULL_POINTER;
     if (tab->weights == nullptr || tab->table_offset == nullptr || tab->table_offset_host == nullptr)
         return TBE_ERR_NULL_POINTER;
-    if (tab->T < 1 || tab->D < 1) return TBE_ERR_INVALID_ARGUMENT;
-    if (tab->dtype != TBE_F32 && tab->dtype != TBE_F16 && tab->dtype != TBE_BF16)
+    const bool layouts = tab->layout != nullptr || bt->bag_layout != nullptr;
+    if (tab->T < 1 || (tab->layout == nullptr && tab->D < 1)) return TBE_ERR_INVALID_ARGUMENT;
+    if (tab->layout == nullptr && tab->dtype != TBE_F32 && tab->dtype != TBE_F16 &&
+        tab->dtype != TBE_BF16)
         return TBE_ERR_UNSUPPORTED_DTYPE;
-    if (bt->N < 0 || bt->N >= (int64_t(1) << 30) || bt->B < 0) return TBE_ERR_INVALID_ARGUMENT;
-    if ((int64_t)tab->T * bt->B >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
+    if (bt->N < 0 || bt->N >= (int64_t(1) << 30) || (!layouts && bt->B < 0))
+        return TBE_ERR_INVALID_ARGUMENT;
+    if (!layouts && (int64_t)tab->T * bt->B >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
     if (bt->offsets == nullptr) return TBE_ERR_NULL_POINTER;
     if (bt->N > 0 && bt->indices == nullptr) return TBE_ERR_NULL_POINTER;
     if (bt->index_type != TBE_INDEX_I32 && bt->index_type != TBE_INDEX_I64)
@@ -159,6 +232,14 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     pr->T = tab->T;
     pr->D = tab->D;
     pr->dtype = tab->dtype;
+    pr->layouts = layouts;
+    if (layouts) {
+        const tbe_status ls = check_layouts(tab, bt, pr);
+        if (ls != TBE_OK) return ls;
+    } else {
+        pr->classes.classes.assign(1, TableClass{tab->D, tab->dtype, {}});
+        pr->classes.B.clear();
+    }
     pr->rows_total = rows_total;
     pr->max_rows = max_rows;
     pr->key_bits = bits_for(rows_total);
@@ -174,12 +255,13 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
     pr->max_long = bt->N / c.sl_threshold + 1;
     pr->max_chunks = bt->N / c.chunk + pr->max_long + 1;
     pr->path = 1;
-    if (c.hist_mode != TBE_HIST_OFF && hist_shape_ok(tab, bt, max_rows)) {
+    if (c.hist_mode != TBE_HIST_OFF && !layouts && hist_shape_ok(tab, bt, max_rows)) {
         const bool dense_enough = bt->N >= 64 * pr->NB;   // L >= 64 on average
         if (c.hist_mode == TBE_HIST_FORCE || dense_enough) pr->path = 2;
     } else if (c.hist_mode == TBE_HIST_FORCE) {
         return TBE_ERR_HISTOGRAM_SHAPE;
     }
+    if (layouts) return TBE_OK;   // shapes and sizes checked per table above
     // the generic path reads weight rows and gradient rows as 16-byte vectors
     const int esz = tab->dtype == TBE_F32 ? 4 : 2;
     if (pr->path == 1 && (!row_plan(tab->D, esz).ok || !row_plan(tab->D, 4).ok))
@@ -234,13 +316,20 @@ static MetaLayout meta_layout(const Problem &pr) {
     return m;
 }
 
+// bytes between chunk slots' partials in the workspace: D accumulators of
+// the table's precision, or with layouts the largest D in FP64 (any class)
+static int64_t part_stride(const Problem &pr) {
+    if (pr.layouts) return (int64_t)pr.D * 8;
+    return (int64_t)bwd_partials_bytes(1, pr.D, pr.dtype);
+}
+
 static size_t workspace_size(const tbe_tables *tab, const tbe_batch *bt, const Problem &pr) {
     size_t ws = 256;
     if (pr.path == 1) {
         size_t pre = sort_workspace_bytes(pr.N, pr.key_bits);
         const size_t rle = rle_workspace_bytes(pr.N);
         if (rle > pre) pre = rle;
-        const size_t bwd = bwd_partials_bytes(pr.max_chunks, pr.D, pr.dtype);
+        const size_t bwd = (size_t)pr.max_chunks * part_stride(pr);
         ws = pre > bwd ? pre : bwd;
     } else {
         ws = hist_workspace_bytes(tab, bt);
@@ -406,7 +495,8 @@ tbe_status tbe_forward(const tbe_tables *tables, const tbe_batch *batch, float *
     const bool fused_keys = meta != nullptr && pr.key_bytes == 4;
     st = launch_forward(L, tables, batch, out, fused_keys ? (uint32_t *)meta->keys_a : nullptr,
                         fused_keys ? meta->vals_a : nullptr, fused_keys ? meta->bag_of : nullptr,
-                        (uint64_t)pr.rows_total, dev_status, meta ? meta->counters : nullptr);
+                        (uint64_t)pr.rows_total, dev_status, meta ? meta->counters : nullptr,
+                        pr.classes);
     if (st == TBE_OK && meta != nullptr && !fused_keys)
         st = launch_linearize(L, tables, batch, meta->keys_a, pr.key_bytes, meta->vals_a,
                               meta->bag_of, (uint64_t)pr.rows_total, dev_status, meta->counters);
@@ -469,6 +559,8 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_tables *tables, const tbe_batc
     a.sl_threshold = pr.sl_threshold;
     a.chunk = pr.chunk;
     a.long_mode = pr.long_mode;
+    a.classes = &pr.classes;
+    a.part_stride = part_stride(pr);
     return finish(L, launch_backward(L, a));
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "tbe.h"
 
 namespace tbe {
@@ -115,6 +117,49 @@ __device__ __forceinline__ int table_of_key(const int64_t *table_offset, int T, 
     return lo;
 }
 
+// ---- addressing of tables, bags and output rows ---------------------------
+// Uniform problems (no layouts): table t's rows are rows table_offset[t].. of
+// one [rows_total, D] array, bag (t,b) is CSR bag t*B+b and its output row
+// starts at (b*T + t)*D.  With layouts (tables of different D/dtype, or a
+// different B per table) these come from the caller's per-table records.
+
+// byte offset in the weights of element 0 of linearised row `row` of table t
+// (D and esize: the row length and element size of t)
+__device__ __forceinline__ int64_t weight_byte(const tbe_table_layout *layout,
+                                               const int64_t *table_offset, int t, int64_t row,
+                                               int D, int esize) {
+    if (layout == nullptr) return row * D * esize;
+    return __ldg(&layout[t].weights_byte_offset) + (row - __ldg(table_offset + t)) * D * esize;
+}
+
+// float index in out / grad_out of bag b of table t
+__device__ __forceinline__ int64_t out_row(const tbe_bag_layout *bags, int T, int D, int t,
+                                           int64_t b) {
+    if (bags == nullptr) return (b * T + t) * (int64_t)D;
+    return __ldg(&bags[t].out_offset) + b * __ldg(&bags[t].out_stride);
+}
+
+// first CSR bag of table t
+__device__ __forceinline__ int64_t bag_base(const tbe_bag_layout *bags, int64_t B, int t) {
+    return bags == nullptr ? (int64_t)t * B : __ldg(&bags[t].bag_offset);
+}
+
+// table of CSR bag g
+__device__ __forceinline__ int table_of_bag(const tbe_bag_layout *bags, int64_t B, int T, int64_t g) {
+    if (bags == nullptr) return (int)(g / B);
+    int lo = 0, hi = T;   // largest t with bag_offset[t] <= g
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(&bags[mid].bag_offset) <= g) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// whether table t has the row length and dtype of this launch's class
+__device__ __forceinline__ bool in_class(const tbe_table_layout *layout, int t, int D, int dtype) {
+    return layout == nullptr || (__ldg(&layout[t].D) == D && __ldg(&layout[t].dtype) == dtype);
+}
+
 // ---------------------------------------------------------------------------
 // Host-side launch context: the caller's stream, config and optional
 // per-kernel timing events.
@@ -147,12 +192,24 @@ struct RowPlan {
 };
 RowPlan row_plan(int D, int bytes_per_elem);
 
+// Host-side grouping of tables with layouts into launch classes of one row
+// length and dtype (uniform problems: one class of all tables).
+struct TableClass {
+    int D, dtype;
+    std::vector<int> tables;
+};
+struct TableClasses {
+    std::vector<TableClass> classes;
+    std::vector<int64_t> B;   // bags of each table
+};
+
 // --- forward.cu
 // `counters` (nullable) receives C_MALFORMED / C_DECREASING.  `keys`
-// (nullable) are 32-bit: 64-bit keys come from launch_linearize.
+// (nullable) are 32-bit: 64-bit keys come from launch_linearize.  Tables
+// with layouts are gathered one class per launch.
 tbe_status launch_forward(Launch &L, const tbe_tables *tab, const tbe_batch *bt, float *out,
                           uint32_t *keys, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
-                          int32_t *status, int32_t *counters);
+                          int32_t *status, int32_t *counters, const TableClasses &cls);
 tbe_status launch_linearize(Launch &L, const tbe_tables *tab, const tbe_batch *bt, void *keys,
                             int key_bytes, uint32_t *vals, int32_t *bag_of, uint64_t sentinel,
                             int32_t *status, int32_t *counters);
@@ -229,6 +286,8 @@ struct BwdArgs {
     int32_t *status;         // caller's device status words
     int64_t max_chunks, max_long;
     int sl_threshold, chunk, long_mode;
+    const TableClasses *classes;   // the launch classes (one for uniform problems)
+    int64_t part_stride;           // bytes between chunk slots' partials
 };
 size_t bwd_partials_bytes(int64_t max_chunks, int D, int dtype);
 tbe_status launch_backward(Launch &L, const BwdArgs &a);

@@ -57,12 +57,27 @@ class tbe_config(ctypes.Structure):
 
 class tbe_tables(ctypes.Structure):
     _fields_ = [("weights", P), ("table_offset", P), ("table_offset_host", P), ("T", i32),
-                ("D", i32), ("dtype", i32)]
+                ("D", i32), ("dtype", i32), ("layout", P), ("layout_host", P)]
 
 
 class tbe_batch(ctypes.Structure):
     _fields_ = [("indices", P), ("offsets", P), ("N", i64), ("B", i64),
-                ("per_sample_weights", P), ("weighted_tables", P), ("index_type", i32)]
+                ("per_sample_weights", P), ("weighted_tables", P), ("index_type", i32),
+                ("bag_layout", P), ("bag_layout_host", P), ("out_size", i64)]
+
+
+# tbe_table_layout and tbe_bag_layout records, as numpy structured dtypes
+TABLE_LAYOUT = np.dtype([("weights_byte_offset", np.int64), ("D", np.int32), ("dtype", np.int32)])
+BAG_LAYOUT = np.dtype([("bag_offset", np.int64), ("B", np.int64), ("out_offset", np.int64),
+                       ("out_stride", np.int64)])
+DTYPE_NAMES = {"f32": F32, "f16": F16, "bf16": BF16}
+
+
+def _records(host: np.ndarray, device) -> tuple:
+    """A host array of records and its device copy (raw bytes)."""
+    host = np.ascontiguousarray(host)
+    dev = torch.from_numpy(host.view(np.uint8).copy()).to(device)
+    return host, dev
 
 
 class tbe_meta(ctypes.Structure):
@@ -144,18 +159,35 @@ def config(sl_threshold: int = 256, chunk: int = 256, long_run_mode: int = LONG_
 
 
 class Tables:
-    """T tables stored back to back: weights [rows_total, D] on the device."""
+    """T embedding tables on the device.
 
-    def __init__(self, weights: torch.Tensor, table_offset: Sequence[int]):
-        assert weights.is_cuda and weights.dim() == 2 and weights.is_contiguous()
+    Uniform: weights [rows_total, D] of one dtype, tables back to back.
+    With ``layout`` (one dict per table with keys wbyte, D, dtype -- dtype
+    'f32', 'f16' or 'bf16'): weights is a byte buffer and table t's rows of
+    D_t elements of its dtype start at byte wbyte."""
+
+    def __init__(self, weights: torch.Tensor, table_offset: Sequence[int], layout=None):
+        assert weights.is_cuda and weights.is_contiguous()
         self.weights = weights
         self.table_offset_host = np.ascontiguousarray(np.asarray(table_offset, dtype=np.int64))
         self.table_offset = torch.from_numpy(self.table_offset_host).to(weights.device)
         self.T = len(self.table_offset_host) - 1
-        self.D = weights.shape[1]
+        self.layout_host = self.layout_dev = None
+        if layout is None:
+            assert weights.dim() == 2
+            self.D = weights.shape[1]
+            dt = _TORCH_DTYPE[weights.dtype]
+            lay = lay_h = None
+        else:
+            rec = np.zeros(self.T, TABLE_LAYOUT)
+            for t, L in enumerate(layout):
+                rec[t] = (L["wbyte"], L["D"], DTYPE_NAMES[L["dtype"]])
+            self.layout_host, self.layout_dev = _records(rec, weights.device)
+            self.D = int(rec["D"].max())
+            dt = F32
+            lay, lay_h = self.layout_dev.data_ptr(), self.layout_host.ctypes.data
         self.c = tbe_tables(weights.data_ptr(), self.table_offset.data_ptr(),
-                            self.table_offset_host.ctypes.data, self.T, self.D,
-                            _TORCH_DTYPE[weights.dtype])
+                            self.table_offset_host.ctypes.data, self.T, self.D, dt, lay, lay_h)
 
     def refresh(self):
         self.c.weights = self.weights.data_ptr()
@@ -163,18 +195,33 @@ class Tables:
 
 class Batch:
     """One KeyedJagged CSR batch on the device: indices and offsets both int32
-    or both int64."""
+    or both int64.
+
+    With ``bag_layout`` (one dict per table with keys bag_off, B, out_off,
+    stride) each table has its own number of bags and its bags' output rows
+    lie at out[out_off + b*stride] of a flat out of ``out_size`` floats (B is
+    then ignored); required for tables with a layout."""
 
     def __init__(self, indices: torch.Tensor, offsets: torch.Tensor, B: int,
                  per_sample_weights: Optional[torch.Tensor] = None,
-                 weighted_tables: Optional[torch.Tensor] = None):
+                 weighted_tables: Optional[torch.Tensor] = None, bag_layout=None,
+                 out_size: int = 0):
         assert indices.dtype == offsets.dtype and indices.dtype in (torch.int32, torch.int64)
         self.indices, self.offsets, self.B = indices, offsets, int(B)
         self.per_sample_weights, self.weighted_tables = per_sample_weights, weighted_tables
         self.N = int(indices.numel())
         itype = INDEX_I64 if indices.dtype == torch.int64 else INDEX_I32
+        self.bag_layout_host = self.bag_layout_dev = None
+        self.out_size = int(out_size)
+        bl = bl_h = None
+        if bag_layout is not None:
+            rec = np.zeros(len(bag_layout), BAG_LAYOUT)
+            for t, L in enumerate(bag_layout):
+                rec[t] = (L["bag_off"], L["B"], L["out_off"], L["stride"])
+            self.bag_layout_host, self.bag_layout_dev = _records(rec, indices.device)
+            bl, bl_h = self.bag_layout_dev.data_ptr(), self.bag_layout_host.ctypes.data
         self.c = tbe_batch(_ptr(indices), _ptr(offsets), self.N, self.B, _ptr(per_sample_weights),
-                           _ptr(weighted_tables), itype)
+                           _ptr(weighted_tables), itype, bl, bl_h, self.out_size)
 
 
 def tbe_query_sizes(tables: Tables, batch: Batch, cfg: Optional[tbe_config] = None):
@@ -276,8 +323,9 @@ class TBE:
 
     def forward(self, batch: Batch, out: Optional[torch.Tensor] = None, stream=None):
         if out is None:
-            out = torch.empty((batch.B, self.tables.T * self.tables.D), dtype=torch.float32,
-                              device=self.tables.weights.device)
+            shape = (batch.out_size,) if batch.bag_layout_host is not None else \
+                (batch.B, self.tables.T * self.tables.D)
+            out = torch.empty(shape, dtype=torch.float32, device=self.tables.weights.device)
         meta = self.meta if (self.preprocess_in_forward or self.path == 2) else None
         tbe_forward(self.tables, batch, out, meta, self.workspace, self.status, self.cfg, stream)
         return out

@@ -181,12 +181,23 @@ def assert_weights_close(dev_bits: np.ndarray, ref_bits: np.ndarray, old_bits: n
                              f"ref={r[i]!r} old={o[i]!r} bound={bound[i]!r}")
 
 
+def bag_tables(wl, g: np.ndarray) -> np.ndarray:
+    """Table of each CSR bag id."""
+    starts = np.array([L["bag_off"] for L in wl.layout()], np.int64)
+    return np.searchsorted(starts, g, side="right") - 1
+
+
 def touched_rows(wl) -> np.ndarray:
-    tab = (np.searchsorted(wl.offsets, np.arange(wl.N), side="right") - 1) // wl.B
+    tab = bag_tables(wl, np.searchsorted(wl.offsets, np.arange(wl.N), side="right") - 1)
     ok = (wl.indices >= 0) & (wl.indices < wl.table_rows[tab])
     t = np.zeros(wl.rows_total, bool)
     t[(wl.table_offset[tab] + wl.indices)[ok]] = True
     return t
+
+
+def shaped(wl) -> bool:
+    """Tables of different D or dtype (weights in one byte buffer)."""
+    return wl.table_dims is not None or wl.table_dtypes is not None
 
 
 def device_batch(wl, device="cuda"):
@@ -195,7 +206,31 @@ def device_batch(wl, device="cuda"):
     off = torch.from_numpy(wl.offsets).to(device)
     psw = torch.from_numpy(wl.per_sample_weights).to(device) if wl.per_sample_weights is not None else None
     wt = torch.from_numpy(wl.weighted_tables).to(device) if wl.weighted_tables is not None else None
+    if wl.mixed:
+        return Batch(idx, off, wl.B, psw, wt, bag_layout=wl.layout(), out_size=wl.out_size)
     return Batch(idx, off, wl.B, psw, wt)
+
+
+def table_storage(wl, W: np.ndarray, t: int) -> np.ndarray:
+    """Table t's rows [E_t, D_t] as stored (float32, or uint16 bits) out of a
+    weight buffer (bytes laid out as wl.layout(), or a uniform array)."""
+    L = wl.layout()[t]
+    E = int(wl.table_rows[t])
+    if W.dtype != np.uint8:
+        to = wl.table_offset
+        return W[to[t]:to[t + 1]]
+    nbytes = E * L["D"] * (4 if L["dtype"] == "f32" else 2)
+    raw = W[L["wbyte"]:L["wbyte"] + nbytes]
+    return raw.view(np.float32 if L["dtype"] == "f32" else np.uint16).reshape(E, L["D"])
+
+
+def table_out(wl, out: np.ndarray, t: int) -> np.ndarray:
+    """Table t's pooled rows [B_t, D_t] out of a flat out / grad_out."""
+    L = wl.layout()[t]
+    flat = out.reshape(-1)
+    if wl.vbe:
+        return flat[L["out_off"]:L["out_off"] + L["B"] * L["D"]].reshape(L["B"], L["D"])
+    return flat.reshape(wl.B, -1)[:, L["out_off"]:L["out_off"] + L["D"]]
 
 
 def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
@@ -204,8 +239,12 @@ def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
     meta_fill (a byte value) fills the metadata buffer before the first call,
     in place of whatever a fresh device allocation holds."""
     from recsys_table_embedding_gb300 import TBE, Tables, meta_view
-    W = W0.to(device).contiguous()
-    tables = Tables(W, wl.table_offset)
+    if isinstance(W0, np.ndarray):       # a byte buffer of tables of different shapes
+        W = torch.from_numpy(W0).to(device)
+        tables = Tables(W, wl.table_offset, layout=wl.layout())
+    else:
+        W = W0.to(device).contiguous()
+        tables = Tables(W, wl.table_offset)
     batch = device_batch(wl, device)
     tbe = TBE(tables, batch, cfg, preprocess_in_forward=preprocess_in_forward)
     if meta_fill is not None:
@@ -215,7 +254,8 @@ def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
     Gd = torch.from_numpy(G).to(device)
     tbe.backward(batch, mom, Gd, wl.lr, wl.eps)
     torch.cuda.synchronize()
-    res = dict(out=out.cpu().numpy(), W=wbits_np(W, wl.dtype), mom=mom.cpu().numpy(),
+    Wh = W.cpu().numpy() if W.dtype == torch.uint8 else wbits_np(W, wl.dtype)
+    res = dict(out=out.cpu().numpy(), W=Wh, mom=mom.cpu().numpy(),
                status=tbe.status.cpu().numpy(), path=tbe.path, tbe=tbe)
     if tbe.path == 1:
         m = tbe.meta
@@ -256,7 +296,9 @@ def check_inversion(wl, res, pre):
         np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64), pre["sorted_pos"])
     else:
         bag = bag_of_position(wl, pre["sorted_pos"])
-        np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64), bag % wl.B)
+        starts = np.array([L["bag_off"] for L in wl.layout()], np.int64)
+        np.testing.assert_array_equal(res["sorted_vals"][:nv].astype(np.int64),
+                                      bag - starts[bag_tables(wl, bag)])
     np.testing.assert_array_equal(res["unique_keys"].astype(np.int64), pre["unique_keys"])
     np.testing.assert_array_equal(res["seg_off"].astype(np.int64), pre["seg_off"])
     rl = pre["run_len"]
@@ -264,11 +306,18 @@ def check_inversion(wl, res, pre):
     assert res["num_chunks"] == int(((rl[rl >= 256] + 255) // 256).sum())
 
 
-def check_full(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, res: dict, pre=None):
-    """Compare a full CUDA step with the oracle: forward, inversion, backward."""
-    wb = wbits_np(W0, wl.dtype)
+def check_full(wl, W0, G: np.ndarray, m0: np.ndarray, res: dict, pre=None):
+    """Compare a full CUDA step with the oracle: forward, inversion, backward.
+    W0: the initial weights (torch tensor, or the byte buffer of tables of
+    different shapes)."""
+    wb = W0 if isinstance(W0, np.ndarray) else wbits_np(W0, wl.dtype)
     out, ab, oob, bad = oracle.forward(wl, wb, want_abs=True)
-    assert_out_close(res["out"], out, ab, wl.dtype)
+    if wl.mixed:
+        for t in range(wl.T):
+            assert_out_close(table_out(wl, res["out"], t), table_out(wl, out, t), table_out(wl, ab, t),
+                             wl.dtype_t(t))
+    else:
+        assert_out_close(res["out"], out, ab, wl.dtype)
     assert int(res["status"][0]) == oob
     malformed = oracle.offsets_check(wl)[0]
     assert bool(res["status"][1] & 0x1) == malformed, "TBE_FLAG_BAD_OFFSETS"
@@ -284,6 +333,15 @@ def check_full(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, res: dict, p
     assert U == int(touched.sum())
     assert_momentum_close(res["mom"], mn, m0, touched)
     k = runs["keys"]
-    arith = w_arith_bound(wl.dtype, runs["grad"], runs["abs"], runs["count"], m0[k],
-                          wvals_np(wb[k], wl.dtype), wl.lr, wl.eps, res["path"])
-    assert_weights_close(res["W"], Wn, wb, touched, wl.dtype, arith)
+    to = wl.table_offset
+    for t in range(wl.T if wl.mixed else 1):
+        # one table at a time (all at once when they share D and dtype)
+        lo, hi = (to[t], to[t + 1]) if wl.mixed else (0, wl.rows_total)
+        sel = (k >= lo) & (k < hi)
+        dt, D = (wl.dtype_t(t), wl.Dt(t)) if wl.mixed else (wl.dtype, wl.D)
+        old = table_storage(wl, wb, t) if wl.mixed else wb
+        arith = w_arith_bound(dt, runs["grad"][sel][:, :D], runs["abs"][sel][:, :D], runs["count"][sel],
+                              m0[k[sel]], wvals_np(old[k[sel] - lo], dt), wl.lr, wl.eps, res["path"])
+        dev = table_storage(wl, res["W"], t) if wl.mixed else res["W"]
+        ref = table_storage(wl, Wn, t) if wl.mixed else Wn
+        assert_weights_close(dev, ref, old, touched[lo:hi], dt, arith)
