@@ -1108,7 +1108,9 @@ tbe_status launch_backward(Launch &L, const BwdArgs &a) {
     p.counters = m->counters;
     p.long_run = m->long_run;
     p.long_chunk_base = m->long_chunk_base;
-    p.chunk_order = chunk_order_on(a.bt->B, a.tab->T) ? m->chunk_order : nullptr;
+    // the order the RLE built (none for batches with a bag layout)
+    p.chunk_order = a.bt->bag_layout == nullptr && chunk_order_on(a.bt->B, a.tab->T) ? m->chunk_order
+                                                                                      : nullptr;
     p.chunk_desc = m->chunk_desc;
     p.partials = a.partials;
     p.arrive = a.arrive;

@@ -445,7 +445,12 @@ static FwdParams make_params(const tbe_tables *tab, const tbe_batch *bt, float *
     p.status = status;
     p.counters = counters;
     p.B = bt->B;
+    // with a bag layout the bags are counted per table (B is ignored)
     p.NB = (int64_t)tab->T * bt->B;
+    if (bt->bag_layout_host != nullptr) {
+        p.NB = 0;
+        for (int t = 0; t < tab->T; ++t) p.NB += bt->bag_layout_host[t].B;
+    }
     p.N = bt->N;
     p.T = tab->T;
     p.D = tab->D;

@@ -277,7 +277,7 @@ tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws) {
     const int64_t ntiles = (a.N + RLE_TILE - 1) / RLE_TILE;
     int32_t *tile_heads = (int32_t *)ws;
     int32_t *win = (int32_t *)((char *)ws + ((size_t)(ntiles + 1) * 4 + 255) / 256 * 256);
-    const bool order = chunk_order_on(a.B, a.T);
+    const bool order = a.order_ok && chunk_order_on(a.B, a.T);
     const int wshift = order ? chunk_window_shift(a.B, a.T) : -1;
     const int nwin = order ? a.T * (int)((a.B + (int64_t(1) << wshift) - 1) >> wshift) : 0;
     L.before("tbe_rle_count");

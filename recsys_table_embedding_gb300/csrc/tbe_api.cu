@@ -385,6 +385,7 @@ static tbe_status run_inversion(Launch &L, const tbe_tables *tab, const tbe_batc
     a.T = tab->T;
     a.sl_threshold = pr.sl_threshold;
     a.chunk = pr.chunk;
+    a.order_ok = bt->bag_layout == nullptr;
     return launch_rle(L, a, ws);
 }
 

@@ -270,6 +270,7 @@ struct RleArgs {
     int T;
     int sl_threshold;
     int chunk;
+    bool order_ok;   // chunk ordering by bag window applies (every table has B bags)
 };
 tbe_status launch_rle(Launch &L, const RleArgs &a, void *ws);
 
