@@ -76,23 +76,34 @@ __device__ __forceinline__ int64_t load_key(const BwdParams &p, int64_t r) {
                    : (int64_t)__ldg(reinterpret_cast<const uint32_t *>(p.unique_keys) + r);
 }
 
-// weight row of linearised row `key` of table t (row length p.D)
-template <typename WT> __device__ __forceinline__ WT *wrow_of(const BwdParams &p, int t, int64_t key) {
+// weight row of linearised row `key` of table t (row length p.D); `layout`
+// is p.layout, or a null constant where a kernel is built without layouts
+template <typename WT>
+__device__ __forceinline__ WT *wrow_of(const BwdParams &p, const tbe_table_layout *layout, int t,
+                                       int64_t key) {
     return reinterpret_cast<WT *>(reinterpret_cast<char *>(p.W) +
-                                  weight_byte(p.layout, p.table_offset, t, key, p.D, (int)sizeof(WT)));
+                                  weight_byte(layout, p.table_offset, t, key, p.D, (int)sizeof(WT)));
+}
+template <typename WT> __device__ __forceinline__ WT *wrow_of(const BwdParams &p, int t, int64_t key) {
+    return wrow_of<WT>(p, p.layout, t, key);
 }
 
 // bag within table t of a sorted payload: the bag itself (unweighted
 // batches) or, for a lookup position, its CSR bag less the table's first
-__device__ __forceinline__ int64_t payload_bag(const BwdParams &p, uint32_t v, int t) {
+__device__ __forceinline__ int64_t payload_bag(const BwdParams &p, const tbe_bag_layout *bags,
+                                               uint32_t v, int t) {
     if (!p.payload_pos) return (int64_t)v;
-    return (int64_t)__ldg(p.bag_of + v) - bag_base(p.bag_layout, p.B, t);
+    return (int64_t)__ldg(p.bag_of + v) - bag_base(bags, p.B, t);
+}
+__device__ __forceinline__ int64_t payload_bag(const BwdParams &p, uint32_t v, int t) {
+    return payload_bag(p, p.bag_layout, v, t);
 }
 
 // bags of table t
-__device__ __forceinline__ int64_t bags_of(const BwdParams &p, int t) {
-    return p.bag_layout == nullptr ? p.B : __ldg(&p.bag_layout[t].B);
+__device__ __forceinline__ int64_t bags_of(const BwdParams &p, const tbe_bag_layout *bags, int t) {
+    return bags == nullptr ? p.B : __ldg(&bags[t].B);
 }
+__device__ __forceinline__ int64_t bags_of(const BwdParams &p, int t) { return bags_of(p, p.bag_layout, t); }
 
 __device__ __forceinline__ void acc4(double (&a)[4], const float4 x, float w) {
     a[0] = fma((double)w, (double)x.x, a[0]);
@@ -359,9 +370,12 @@ __device__ __forceinline__ void unpack(const typename WRaw<WT>::t r, float (&w)[
 // gl + q*GL (q < NV) of the row (float4 of the gradient, 4 weights).  The
 // weight slice and the momentum are loaded before the gather so their
 // latency overlaps it; U gradient rows of the run are in flight per step.
-template <typename WT, int GL, int NV, int U>
+template <typename WT, int GL, int NV, int U, bool LAY>
 __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
+    // LAY: tables or bags with layouts; without, the layout code folds away
+    const tbe_table_layout *layout = LAY ? p.layout : nullptr;
+    const tbe_bag_layout *bag_layout = LAY ? p.bag_layout : nullptr;
     constexpr int GPW = 32 / GL;
     const int lane = threadIdx.x & 31, grp = lane / GL, gl = lane % GL;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -378,8 +392,11 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
             key = load_key(p, r);
         }
         bool mine = r < U_runs && e - s < p.sl_threshold;
-        const int t = mine ? table_of_key(p.table_offset, p.T, key) : 0;
-        mine = mine && in_class(p.layout, t, p.D, p.cls_dtype);
+        int t = 0;
+        if (layout != nullptr) {   // the run's table decides its class first
+            if (mine) t = table_of_key(p.table_offset, p.T, key);
+            mine = mine && in_class(layout, t, p.D, p.cls_dtype);
+        }
         ACC acc[NV][4];
 #pragma unroll
         for (int q = 0; q < NV; ++q)
@@ -387,19 +404,23 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
         typename WRaw<WT>::t wraw[NV];
         float m_old = 0.f;
-        WT *wr = mine ? wrow_of<WT>(p, t, key) : nullptr;
+        // uniform tables: the weight row follows from the key alone, so its
+        // loads are issued before the table lookup
+        WT *wr = layout != nullptr ? (mine ? wrow_of<WT>(p, layout, t, key) : nullptr)
+                                   : reinterpret_cast<WT *>(p.W) + key * p.D;
         if (mine) {
 #pragma unroll
             for (int q = 0; q < NV; ++q) wraw[q] = ld_wraw(wr + (gl + q * GL) * 4);
             m_old = p.mom[key];
+            if (layout == nullptr) t = table_of_key(p.table_offset, p.T, key);
             const bool wt = p.psw != nullptr && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
             // gradient row of bag b: G + g0 + b * gs
-            const float *Gt = p.G + (p.bag_layout ? __ldg(&p.bag_layout[t].out_offset) : (int64_t)t * p.D) +
+            const float *Gt = p.G + (bag_layout ? __ldg(&bag_layout[t].out_offset) : (int64_t)t * p.D) +
                               gl * 4;
-            const int64_t gs = p.bag_layout ? __ldg(&p.bag_layout[t].out_stride) : TD;
-            const int64_t Bt = bags_of(p, t);
+            const int64_t gs = bag_layout ? __ldg(&bag_layout[t].out_stride) : TD;
+            const int Bt = (int)bags_of(p, bag_layout, t);
             for (int32_t i = s; i < e; i += U) {
-                int64_t bk[U];
+                int bk[U];
                 float wk[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -407,7 +428,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
                     wk[u] = 1.f;
                     if (i + u < e) {
                         const uint32_t v = __ldg(p.vals + i + u);
-                        const int64_t b = payload_bag(p, v, t);
+                        const int b = (int)payload_bag(p, bag_layout, v, t);
                         if (p.payload_pos && wt) wk[u] = __ldg(p.psw + v);
                         // only malformed (overlapping) offsets can give a bag
                         // outside the run's table; such a lookup adds nothing
@@ -420,7 +441,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
                     if (bk[u] >= 0)
 #pragma unroll
                         for (int q = 0; q < NV; ++q)
-                            x[u][q] = __ldg(reinterpret_cast<const float4 *>(Gt + bk[u] * gs + q * GL * 4));
+                            x[u][q] = __ldg(reinterpret_cast<const float4 *>(Gt + (int64_t)bk[u] * gs + q * GL * 4));
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     if (bk[u] >= 0)
@@ -697,9 +718,12 @@ struct SsTask {
     float mom;      // momentum of the lane's row
 };
 
-template <typename WT, int NV>
+template <typename WT, int NV, bool LAY>
 __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
+    // LAY: tables or bags with layouts; without, the layout code folds away
+    const tbe_table_layout *layout = LAY ? p.layout : nullptr;
+    const tbe_bag_layout *bag_layout = LAY ? p.bag_layout : nullptr;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -747,8 +771,11 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
     uint32_t wphase = 0;   // bit k: parity of weight buffer k's next completion
     auto task_prepare = [&](SsTask &T, int wb) {
         bool mine = T.q >= 0 && lane < T.nr && T.e - T.s < p.sl_threshold;
-        const int tt = mine ? table_of_key(p.table_offset, p.T, T.key) : 0;
-        mine = mine && in_class(p.layout, tt, p.D, p.cls_dtype);
+        int tt = 0;
+        if (layout != nullptr) {   // the run's table decides its class first
+            if (mine) tt = table_of_key(p.table_offset, p.T, T.key);
+            mine = mine && in_class(layout, tt, p.D, p.cls_dtype);
+        }
         T.len = mine ? T.e - T.s : 0;
         int x = T.len;
 #pragma unroll
@@ -758,15 +785,15 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
         }
         T.total = __shfl_sync(FULL, x, 31);
         T.pre = x - T.len;
-        T.t = mine ? tt : 0;
         T.mom = mine ? p.mom[T.key] : 0.f;
+        T.t = !mine ? 0 : (layout != nullptr ? tt : table_of_key(p.table_offset, p.T, T.key));
         const unsigned m = __ballot_sync(FULL, mine);
         if (m) {
             const uint32_t bar = wbar0 + 8 * wb;
             if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)__popc(m) * (uint32_t)wrow);
             __syncwarp();
             if (mine)
-                bulk_g2s(smem_addr(wbuf + wb * SS_WBUF + lane * wrow), wrow_of<WT>(p, T.t, T.key),
+                bulk_g2s(smem_addr(wbuf + wb * SS_WBUF + lane * wrow), wrow_of<WT>(p, layout, T.t, T.key),
                          (uint32_t)wrow, bar);
         }
     };
@@ -788,16 +815,16 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
         const int t_sl = __shfl_sync(FULL, T.t, slot);
         if (k < T.total) {
             const uint32_t v = __ldg(p.vals + s_sl + (k - pre_sl));
-            const int64_t b = payload_bag(p, v, t_sl);
+            const int64_t b = payload_bag(p, bag_layout, v, t_sl);
             float x = 1.f;
             if (p.payload_pos && p.psw != nullptr &&
                 (p.weighted == nullptr || __ldg(p.weighted + t_sl) != 0))
                 x = __ldg(p.psw + v);
             // only malformed (overlapping) offsets can give a bag outside the
             // run's table: such a lookup copies row 0 with weight 0
-            const bool ok = b >= 0 && b < bags_of(p, t_sl);
-            const int64_t g0 = p.bag_layout ? __ldg(&p.bag_layout[t_sl].out_offset) : (int64_t)t_sl * p.D;
-            const int64_t gs = p.bag_layout ? __ldg(&p.bag_layout[t_sl].out_stride) : TD;
+            const bool ok = b >= 0 && b < bags_of(p, bag_layout, t_sl);
+            const int64_t g0 = bag_layout ? __ldg(&bag_layout[t_sl].out_offset) : (int64_t)t_sl * p.D;
+            const int64_t gs = bag_layout ? __ldg(&bag_layout[t_sl].out_stride) : TD;
             tab_off[tb * SS_BLK + lane] = ok ? (uint32_t)((g0 + b * gs) >> 2) : 0u;
             tab_w[tb * SS_BLK + lane] = ok ? x : 0.f;
             tab_tag[tb * SS_BLK + lane] = (uint32_t)slot | (k == pre_sl + len_sl - 1 ? SS_LAST : 0u);
@@ -940,7 +967,7 @@ __global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(con
                 const float m_new = A::mom(m_old, ss, p.D);
                 const auto den = A::den(m_new, p.eps);
                 const WT *wsrc = reinterpret_cast<const WT *>(wbuf + cw * SS_WBUF + slot * wrow) + lane * 4;
-                WT *wdst = wrow_of<WT>(p, tk, key) + lane * 4;
+                WT *wdst = wrow_of<WT>(p, layout, tk, key) + lane * 4;
 #pragma unroll
                 for (int q = 0; q < NV; ++q) {
                     float w[4];
@@ -1048,7 +1075,8 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         // position payload (2.60 vs 2.82 ms on the mid workload, while the
         // register kernel stays ahead on unweighted batches, 2.55 vs 2.80 ms
         // on the large one)
-        auto ks = tbe_bwd_short_stream_kernel<WT, NV>;
+        auto ks = (p.layout != nullptr || p.bag_layout != nullptr) ? tbe_bwd_short_stream_kernel<WT, NV, true>
+                                                                   : tbe_bwd_short_stream_kernel<WT, NV, false>;
         const size_t ssm = (size_t)SS_WARPS * ss_warp_bytes();
         cached_smem_attr(L.dev, (const void *)ks, ssm);
         L.before("tbe_bwd_short_run");
@@ -1062,7 +1090,8 @@ static void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         constexpr int SGL = V / SNV;
         static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0, "short-run lane groups");
         constexpr int SU = SNV >= 3 ? 2 : 4;
-        auto ks = tbe_bwd_short_kernel<WT, SGL, SNV, SU>;
+        auto ks = (p.layout != nullptr || p.bag_layout != nullptr) ? tbe_bwd_short_kernel<WT, SGL, SNV, SU, true>
+                                                                   : tbe_bwd_short_kernel<WT, SGL, SNV, SU, false>;
         L.before("tbe_bwd_short_run");
         ks<<<persistent_grid(L, ks), 256, 0, L.stream>>>(p);
         L.after();

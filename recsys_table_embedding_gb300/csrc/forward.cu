@@ -151,8 +151,13 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 // without predicates or branches; the rest of a 32-lookup block (and any
 // block with an out-of-range index) goes one 32/LPR-row step at a time with
 // per-row checks.  (t, b) of the next bag are stepped, not divided.
-template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED, typename IdxT>
+template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED, typename IdxT, bool LAY>
 __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ FwdParams p) {
+    // LAY: tables or bags with layouts, one class of tables per launch;
+    // without, the layout code folds away
+    const int ntl = LAY ? p.ntl : 0;
+    const tbe_table_layout *layout = LAY ? p.layout : nullptr;
+    const tbe_bag_layout *bag_layout = LAY ? p.bag_layout : nullptr;
     using ACC = typename WTraits<WT>::acc;
     constexpr int VEC = VB / (int)sizeof(WT);   // elements per lane vector
     constexpr int RPI = 32 / LPR;
@@ -163,26 +168,26 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
     // division), or bag k of this launch's class tables (table found in the
     // cumulative bag counts)
     int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nitems = p.ntl ? p.tcum[p.ntl] : p.NB;
-    int t = p.ntl ? 0 : (int)(k / p.B);
-    int64_t b = p.ntl ? 0 : k - (int64_t)t * p.B;
-    const int tstep = p.ntl ? 0 : (int)(nwarps / p.B);
-    const int64_t bstep = p.ntl ? 0 : nwarps - (int64_t)tstep * p.B;
+    const int64_t nitems = ntl ? p.tcum[ntl] : p.NB;
+    int t = ntl ? 0 : (int)(k / p.B);
+    int64_t b = ntl ? 0 : k - (int64_t)t * p.B;
+    const int tstep = ntl ? 0 : (int)(nwarps / p.B);
+    const int64_t bstep = ntl ? 0 : nwarps - (int64_t)tstep * p.B;
     int oob = 0;
     check_span<IdxT>(p);
     uint32_t *keys = reinterpret_cast<uint32_t *>(p.keys);
     const IdxT *indices = reinterpret_cast<const IdxT *>(p.indices);
     for (; k < nitems; k += nwarps) {
         int64_t bag = k;
-        if (p.ntl) {
-            int lo = 0, hi = p.ntl;   // class table lo: tcum[lo] <= k < tcum[lo+1]
+        if (ntl) {
+            int lo = 0, hi = ntl;   // class table lo: tcum[lo] <= k < tcum[lo+1]
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (p.tcum[mid] <= k) lo = mid; else hi = mid;
             }
             t = p.tlist[lo];
             b = k - p.tcum[lo];
-            bag = bag_base(p.bag_layout, p.B, t) + b;
+            bag = bag_base(bag_layout, p.B, t) + b;
         }
         const int64_t row0 = __ldg(p.table_offset + t);
         const int64_t E = __ldg(p.table_offset + t + 1) - row0;
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
         read_bag<IdxT>(p, bag, lane, start, end);
         const bool wt = WEIGHTED && (p.weighted == nullptr || __ldg(p.weighted + t) != 0);
         const WT *Wt = reinterpret_cast<const WT *>(reinterpret_cast<const char *>(p.W) +
-                                                    weight_byte(p.layout, p.table_offset, t, row0, p.D,
+                                                    weight_byte(layout, p.table_offset, t, row0, p.D,
                                                                 (int)sizeof(WT))) + li * VEC;
         ACC acc[NV][VEC];
 #pragma unroll
@@ -257,11 +262,11 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) acc[q][e] += __shfl_xor_sync(FULL, acc[q][e], s);
         if (sub == 0) {
-            float *o = p.out + out_row(p.bag_layout, p.T, p.D, t, b) + li * VEC;
+            float *o = p.out + out_row(bag_layout, p.T, p.D, t, b) + li * VEC;
 #pragma unroll
             for (int q = 0; q < NV; ++q) store_out<VEC>(o + q * LPR * VEC, acc[q]);
         }
-        if (!p.ntl) {
+        if (!ntl) {
             t += tstep;
             b += bstep;
             if (b >= p.B) {
@@ -387,11 +392,16 @@ static void fwd_launch(Launch &L, const FwdParams &p) {
     constexpr int US = fwd_unroll<LPR, NV, VB>(TBE_FWD_ROWS);
     constexpr int UL = fwd_unroll<LPR, NV, VB>(2 * TBE_FWD_ROWS);
     const bool long_bags = p.N >= (int64_t)TBE_FWD_LONG_BAG * p.NB;
+    const bool lay = p.ntl != 0;
     auto k = p.psw != nullptr
-                 ? (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, true, IdxT>
-                              : tbe_fwd_kernel<WT, VB, LPR, NV, US, true, IdxT>)
-                 : (long_bags ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false, IdxT>
-                              : tbe_fwd_kernel<WT, VB, LPR, NV, US, false, IdxT>);
+                 ? (long_bags ? (lay ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, true, IdxT, true>
+                                     : tbe_fwd_kernel<WT, VB, LPR, NV, UL, true, IdxT, false>)
+                              : (lay ? tbe_fwd_kernel<WT, VB, LPR, NV, US, true, IdxT, true>
+                                     : tbe_fwd_kernel<WT, VB, LPR, NV, US, true, IdxT, false>))
+                 : (long_bags ? (lay ? tbe_fwd_kernel<WT, VB, LPR, NV, UL, false, IdxT, true>
+                                     : tbe_fwd_kernel<WT, VB, LPR, NV, UL, false, IdxT, false>)
+                              : (lay ? tbe_fwd_kernel<WT, VB, LPR, NV, US, false, IdxT, true>
+                                     : tbe_fwd_kernel<WT, VB, LPR, NV, US, false, IdxT, false>));
     const int grid = grid_for(L, k, 256, p.ntl ? p.tcum[p.ntl] : p.NB);
     L.before("tbe_fwd_gather");
     k<<<grid, 256, 0, L.stream>>>(p);

@@ -88,7 +88,7 @@ def test_malformed_offsets_with_vbe():
     off[-1] = wl.N + 9            # last bag past N
     g = int(np.flatnonzero(np.diff(off) >= 3)[10])
     off[g + 1] = off[g] - 1       # decreasing: no backward update
-    wl.offsets = off
+    wl.offsets = off.astype(np.int32)
     res = _step(wl)
     assert res["status"][1] & 0x1 and res["num_unique"] == 0
 
