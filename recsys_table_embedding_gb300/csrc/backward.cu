@@ -718,8 +718,12 @@ struct SsTask {
     float mom;      // momentum of the lane's row
 };
 
+// 2-byte weights with one vector per lane: registers for 12 CTAs per SM
+// (shared memory allows 12; the kernel is latency-bound), no spill
+template <typename WT, int NV> constexpr int ss_min_blocks() { return sizeof(WT) == 2 && NV == 1 ? 12 : 1; }
+
 template <typename WT, int NV, bool LAY>
-__global__ void __launch_bounds__(SS_WARPS * 32) tbe_bwd_short_stream_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(SS_WARPS * 32, ss_min_blocks<WT, NV>()) tbe_bwd_short_stream_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     // LAY: tables or bags with layouts; without, the layout code folds away
     const tbe_table_layout *layout = LAY ? p.layout : nullptr;
@@ -1043,11 +1047,15 @@ static int persistent_grid(const Launch &L, K kernel, size_t smem = 0, int threa
 }
 
 static constexpr bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-// vectors per lane of the short-run kernel: as many as 4, with a power-of-two group
+#ifndef TBE_SHORT_MAXNV
+#define TBE_SHORT_MAXNV 4   // gradient vectors a lane of the short-run kernel holds per row
+#endif
+// vectors per lane of the short-run kernel: as many as TBE_SHORT_MAXNV, with a
+// power-of-two group of lanes per run
 static constexpr int short_vectors_per_lane(int V) {
-    return (V % 4 == 0 && pow2(V / 4)) ? 4
-           : (V % 3 == 0 && pow2(V / 3)) ? 3
-           : (V % 2 == 0 && pow2(V / 2)) ? 2 : 1;
+    return (TBE_SHORT_MAXNV >= 4 && V % 4 == 0 && pow2(V / 4)) ? 4
+           : (TBE_SHORT_MAXNV >= 3 && V % 3 == 0 && pow2(V / 3)) ? 3
+           : (TBE_SHORT_MAXNV >= 2 && V % 2 == 0 && pow2(V / 2)) ? 2 : 1;
 }
 
 template <typename WT, int LPR, int NV>

@@ -30,8 +30,18 @@ constexpr int MAX_DIGIT_BITS = 9;
 constexpr int RADIX = 1 << MAX_DIGIT_BITS;   // buckets per pass (digits use <= 9 bits)
 constexpr int SORT_THREADS = 512;
 constexpr int SORT_WARPS = SORT_THREADS / 32;
-constexpr int SORT_IPT = 8;
-constexpr int SORT_TILE = SORT_THREADS * SORT_IPT;   // 4096
+#ifndef TBE_SORT_IPT
+#define TBE_SORT_IPT 8   // pairs per thread for 32-bit keys
+#endif
+#ifndef TBE_SORT_LATE_VALS
+#define TBE_SORT_LATE_VALS 0   // 1: payloads are read when scattered, not held through the ranking
+#endif
+// pairs per thread and per tile: 64-bit keys keep 8 per thread (registers)
+template <typename KeyT> struct SortShape {
+    static constexpr int IPT = sizeof(KeyT) == 8 ? 8 : TBE_SORT_IPT;
+    static constexpr int TILE = SORT_THREADS * IPT;
+};
+constexpr int MIN_TILE = SORT_THREADS * 8;   // the workspace is sized for the smallest tile
 constexpr uint32_t ST_AGG = 1u << 30;
 constexpr uint32_t ST_INC = 2u << 30;
 constexpr uint32_t ST_MASK = (1u << 30) - 1;
@@ -54,9 +64,9 @@ struct SortWs {
     int64_t ntiles;
 };
 
-static SortWs carve(void *ws, int64_t N) {
+static SortWs carve(void *ws, int64_t N, int tile) {
     SortWs s;
-    s.ntiles = (N + SORT_TILE - 1) / SORT_TILE;
+    s.ntiles = (N + tile - 1) / tile;
     char *p = (char *)ws;
     s.hist = (uint32_t *)p;
     p += MAX_PASSES * RADIX * 4;
@@ -67,7 +77,7 @@ static SortWs carve(void *ws, int64_t N) {
 }
 
 size_t sort_workspace_bytes(int64_t N, int key_bits) {
-    const int64_t ntiles = (N + SORT_TILE - 1) / SORT_TILE;
+    const int64_t ntiles = (N + MIN_TILE - 1) / MIN_TILE;
     int passes = num_passes(key_bits);
     if (passes < 1) passes = 1;
     return MAX_PASSES * RADIX * 4 + 256 + (size_t)passes * ntiles * RADIX * 4 + 256;
@@ -144,8 +154,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 template <typename KeyT> struct PassSmem {
-    KeyT keys[SORT_TILE];
-    uint32_t vals[SORT_TILE];
+    KeyT keys[SortShape<KeyT>::TILE];
+    uint32_t vals[SortShape<KeyT>::TILE];
     uint32_t warp_cnt[SORT_WARPS][RADIX];   // counts, then exclusive warp prefixes
     uint32_t count[RADIX];
     uint32_t local_off[RADIX];
@@ -160,6 +170,9 @@ radix_onesweep_kernel(const KeyT *__restrict__ keys_in, const uint32_t *__restri
                       KeyT *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t N,
                       int shift, uint32_t mask, const uint32_t *__restrict__ bucket, uint32_t *status,
                       uint32_t *ticket, int32_t *err) {
+    constexpr int IPT = SortShape<KeyT>::IPT;
+    constexpr int TILE = SortShape<KeyT>::TILE;
+    constexpr bool LATE = TBE_SORT_LATE_VALS != 0;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     PassSmem<KeyT> &S = *reinterpret_cast<PassSmem<KeyT> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -168,23 +181,23 @@ radix_onesweep_kernel(const KeyT *__restrict__ keys_in, const uint32_t *__restri
     for (int i = tid; i < SORT_WARPS * RADIX; i += SORT_THREADS) (&S.warp_cnt[0][0])[i] = 0;
     __syncthreads();
     const int64_t tile = S.tile;
-    const int64_t tile_base = tile * SORT_TILE;
+    const int64_t tile_base = tile * TILE;
 
     // warp-striped load: item i of lane l in warp w sits at tile position
     // w*32*IPT + i*32 + l, so (i, lane) order within a warp is input order
-    KeyT k[SORT_IPT];
-    uint32_t v[SORT_IPT], rank[SORT_IPT];
+    KeyT k[IPT];
+    uint32_t v[LATE ? 1 : IPT], rank[IPT];
 #pragma unroll
-    for (int i = 0; i < SORT_IPT; ++i) {
-        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * IPT + i * 32 + lane;
         const bool ok = pos < N;
         k[i] = ok ? __ldg(keys_in + pos) : ~KeyT(0);
-        v[i] = ok ? __ldg(vals_in + pos) : 0u;
+        if constexpr (!LATE) v[i] = ok ? __ldg(vals_in + pos) : 0u;
     }
     const unsigned lt = lanemask_lt();
 #pragma unroll
-    for (int i = 0; i < SORT_IPT; ++i) {
-        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * IPT + i * 32 + lane;
         const uint32_t d = pos < N ? (uint32_t)((k[i] >> shift) & mask) : RADIX;   // RADIX = padding
         const unsigned peers = __match_any_sync(FULL, d);
         const int leader = __ffs(peers) - 1;
@@ -274,19 +287,20 @@ radix_onesweep_kernel(const KeyT *__restrict__ keys_in, const uint32_t *__restri
 
     // reorder the tile by digit in shared memory
 #pragma unroll
-    for (int i = 0; i < SORT_IPT; ++i) {
-        const int64_t pos = tile_base + warp * 32 * SORT_IPT + i * 32 + lane;
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t pos = tile_base + warp * 32 * IPT + i * 32 + lane;
         if (pos < N) {
             const uint32_t d = (uint32_t)((k[i] >> shift) & mask);
             const uint32_t lp = S.local_off[d] + S.warp_cnt[warp][d] + rank[i];
             S.keys[lp] = k[i];
-            S.vals[lp] = v[i];
+            if constexpr (LATE) S.vals[lp] = __ldg(vals_in + pos);
+            else S.vals[lp] = v[i];
         }
     }
     __syncthreads();
 
     const int64_t rem = N - tile_base;
-    const int n = rem < SORT_TILE ? (int)rem : SORT_TILE;
+    const int n = rem < TILE ? (int)rem : TILE;
     for (int j = tid; j < n; j += SORT_THREADS) {
         const KeyT key = S.keys[j];
         const uint32_t d = (uint32_t)((key >> shift) & mask);
@@ -325,7 +339,8 @@ static void sort_passes(Launch &L, KeyT *keys_a, uint32_t *vals_a, KeyT *keys_b,
     L.after();
 
     const size_t smem = sizeof(PassSmem<KeyT>);
-    static_assert(sizeof(PassSmem<uint64_t>) * 2 < 227 * 1024, "pass shared memory");
+    static_assert(sizeof(PassSmem<uint64_t>) * 2 < 227 * 1024 && sizeof(PassSmem<uint32_t>) * 2 < 227 * 1024,
+                  "two pass CTAs per SM");
     cached_smem_attr(L.dev, (const void *)radix_onesweep_kernel<KeyT>, smem);
     const KeyT *ki = keys_a;
     const uint32_t *vi = vals_a;
@@ -357,7 +372,7 @@ tbe_status launch_sort(Launch &L, void *keys_a, uint32_t *vals_a, void *keys_b, 
         return TBE_OK;
     }
     if (passes > MAX_PASSES) return TBE_ERR_KEY_RANGE;
-    const SortWs s = carve(ws, N);
+    const SortWs s = carve(ws, N, key_bytes == 8 ? SortShape<uint64_t>::TILE : SortShape<uint32_t>::TILE);
     if (key_bytes == 8)
         sort_passes<uint64_t>(L, (uint64_t *)keys_a, vals_a, (uint64_t *)keys_b, vals_b, N, passes, bits,
                               s, status);
@@ -375,7 +390,7 @@ tbe_status launch_sort(Launch &L, void *keys_a, uint32_t *vals_a, void *keys_b, 
 // two-tile buffers; the output is invalid, as the flag says).  No copy is in
 // flight during the wait.
 
-constexpr int64_t SELFTEST_N = 2 * SORT_TILE;
+constexpr int64_t SELFTEST_N = 2 * SortShape<uint32_t>::TILE;
 
 size_t sort_selftest_bytes() {
     return (size_t)4 * SELFTEST_N * 4 + RADIX * 4 + 2 * RADIX * 4 + 256;
