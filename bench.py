@@ -145,21 +145,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-KERNEL_SOURCE = [("tbe_fwd_", "forward.cu"), ("tbe_linearize", "forward.cu"),
-                 ("tbe_offsets_fixup", "forward.cu"), ("tbe_sort_", "sort.cu"), ("tbe_rle_", "rle.cu"),
-                 ("tbe_route", "rle.cu"), ("tbe_chunk_", "rle.cu"), ("tbe_zero_counters", "rle.cu"),
-                 ("tbe_bwd_", "backward.cu"), ("tbe_hist_", "hist.cu")]
+_BWD = ("backward.cu", "backward_kernels.cuh", "backward_f32.cu", "backward_f16.cu", "backward_bf16.cu")
+KERNEL_SOURCE = [("tbe_fwd_", ("forward.cu",)), ("tbe_linearize", ("forward.cu",)),
+                 ("tbe_offsets_fixup", ("forward.cu",)), ("tbe_sort_", ("sort.cu",)), ("tbe_rle_", ("rle.cu",)),
+                 ("tbe_route", ("rle.cu",)), ("tbe_chunk_", ("rle.cu",)), ("tbe_zero_counters", ("rle.cu",)),
+                 ("tbe_bwd_", _BWD), ("tbe_hist_", ("hist.cu",))]
 
 
 def src_hash(kernel: str):
-    """Hash of the source file that holds `kernel` and of the shared internal
-    header: an ncu summary is current only while both are unchanged."""
-    fn = next((f for pre, f in KERNEL_SOURCE if kernel.startswith(pre)), None)
-    if fn is None:
+    """Hash of the source files that hold `kernel` and of the shared internal
+    header: an ncu summary is current only while they are unchanged."""
+    fns = next((f for pre, f in KERNEL_SOURCE if kernel.startswith(pre)), None)
+    if fns is None:
         return None
     d = os.path.join(ROOT, "recsys_table_embedding_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (fn, "tbe_internal.cuh"):
+    for f in fns + ("tbe_internal.cuh",):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 

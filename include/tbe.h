@@ -50,6 +50,14 @@
  *    sets TBE_FLAG_BAD_OFFSETS.
  *  - Threading: the functions are reentrant; calls on different streams
  *    must use different workspace and meta buffers.
+ *  - Per-device state: the first call on a device looks up, once, its SM
+ *    count, each kernel's resident blocks per SM and shared-memory limit,
+ *    and (tbe_preprocess_static) the built-in scratch array's address, and
+ *    keeps them for the life of the process.  A process that resets a
+ *    device (cudaDeviceReset) must not call the library on it again.
+ *  - CUDA graphs: the calls enqueue only kernels and event records, so a
+ *    step can be captured; during capture the timing events of
+ *    tbe_config.kernel_events become event-record nodes of the graph.
  */
 #ifndef TBE_GB300_TBE_H
 #define TBE_GB300_TBE_H
@@ -276,7 +284,7 @@ tbe_status tbe_meta_bind(tbe_meta *meta, void *device_buf, size_t bytes,
 /*
  * Forward pooled lookup with fused bounds check (decision checklist item 5):
  * writes out[B, T*D] (device, float32; every element written, empty bags give
- * 0).  Out-of-range indices contribute nothing and are counted into
+ * 0), or, with a bag layout, each bag's row where the layout puts it.  Out-of-range indices contribute nothing and are counted into
  * dev_status[0].  Accumulation is FP32 for FP16/BF16 tables and FP64 for FP32
  * tables (decision checklist item 1).
  * When `meta` is non-NULL the batch inversion also runs here ("Forward state
@@ -300,7 +308,7 @@ tbe_status tbe_preprocess(const tbe_tables *tables, const tbe_batch *batch, tbe_
 /*
  * Backward with the fused exact rowwise Adagrad update ("Backward kernels";
  * TorchEasyRec analysis section 4, fused optimizer).  grad_out is the
- * gradient of `out` (device, float32 [B, T*D]).  Updates tables->weights and
+ * gradient of `out` (device, float32, laid out as out).  Updates tables->weights and
  * momentum (device, float32 [rows_total]) in place, once per touched row;
  * rows no in-range lookup touches are not written.  Runs with SL < 256 take
  * the short-run kernel; longer runs are reduced in 256-lookup chunks (two

@@ -56,6 +56,26 @@ __device__ __forceinline__ int block_excl_scan(int x, int *tot_smem, int &total)
     return wp + y - x;
 }
 
+// the RLE_IPT consecutive keys of one thread from `base` (16-byte vector
+// loads when all are inside the array, `fill` past its end)
+template <typename KeyT>
+__device__ __forceinline__ void load_run_keys(const KeyT *__restrict__ k, int64_t base, int64_t N,
+                                              KeyT fill, KeyT (&kk)[RLE_IPT]) {
+    constexpr int PER = 16 / (int)sizeof(KeyT);   // keys per vector
+    if (base + RLE_IPT <= N) {
+#pragma unroll
+        for (int v = 0; v < RLE_IPT / PER; ++v) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(k + base) + v);
+            const KeyT *e = reinterpret_cast<const KeyT *>(&q);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) kk[v * PER + j] = e[j];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < RLE_IPT; ++i) kk[i] = base + i < N ? __ldg(k + base + i) : fill;
+    }
+}
+
 template <typename KeyT>
 __global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const KeyT *__restrict__ k,
                                                                 int64_t N, KeyT sentinel,
@@ -65,13 +85,15 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const KeyT *__re
     const int64_t base = (int64_t)blockIdx.x * RLE_TILE + threadIdx.x * RLE_IPT;
     int heads = 0;
     KeyT prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : ~KeyT(0);
+    KeyT kk[RLE_IPT];
+    load_run_keys(k, base, N, sentinel, kk);
 #pragma unroll
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
         if (pos < N) {
             // keys >= sentinel (out-of-range lookups and lookups outside every
             // well-formed bag; they sort last) start no run
-            const KeyT cur = __ldg(k + pos);
+            const KeyT cur = kk[i];
             const bool first = pos == 0 || cur != prev;
             if (first && cur < sentinel) ++heads;
             if (cur >= sentinel && (pos == 0 || prev < sentinel)) counters[C_N_VALID] = (int32_t)pos;
@@ -115,10 +137,10 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_write_kernel(
     KeyT kk[RLE_IPT];
     unsigned headmask = 0;
     KeyT prev = base > 0 && base - 1 < N ? __ldg(k + base - 1) : ~KeyT(0);
+    load_run_keys(k, base, N, sentinel, kk);
 #pragma unroll
     for (int i = 0; i < RLE_IPT; ++i) {
         const int64_t pos = base + i;
-        kk[i] = pos < N ? __ldg(k + pos) : sentinel;
         if (pos < N && (pos == 0 || kk[i] != prev) && kk[i] < sentinel) headmask |= 1u << i;
         prev = kk[i];
     }

@@ -170,7 +170,7 @@ static tbe_status check_layouts(const tbe_tables *tab, const tbe_batch *bt, Prob
     if (NB >= (int64_t(1) << 31)) return TBE_ERR_INVALID_ARGUMENT;
     // the backward stages gradient-row offsets as 32-bit counts of 16-byte
     // vectors: grad_out must stay under 64 GB
-    if (bt->out_size / 4 >= (int64_t(1) << 32)) return TBE_ERR_INVALID_ARGUMENT;
+    if (bt->out_size / 4 >= (int64_t(1) << 32) - 1) return TBE_ERR_INVALID_ARGUMENT;
     pr->NB = NB;
     pr->D = Dmax;
     pr->dtype = any32 ? TBE_F32 : TBE_BF16;
@@ -268,7 +268,8 @@ static tbe_status check_problem(const tbe_tables *tab, const tbe_batch *bt, cons
         return TBE_ERR_UNSUPPORTED_DIM;
     // the backward stages gradient-row offsets as 32-bit counts of 16-byte
     // vectors: grad_out must stay under 64 GB
-    if (pr->path == 1 && pr->NB * tab->D / 4 >= (int64_t(1) << 32)) return TBE_ERR_INVALID_ARGUMENT;
+    // (one value short of 2^32: the backward marks a missing row with all ones)
+    if (pr->path == 1 && pr->NB * tab->D / 4 >= (int64_t(1) << 32) - 1) return TBE_ERR_INVALID_ARGUMENT;
     return TBE_OK;
 }
 
