@@ -145,8 +145,8 @@ __device__ __forceinline__ void st4(__half *p, const float (&w)[4]) {
 }
 __device__ __forceinline__ void ld4(const __nv_bfloat16 *p, float (&w)[4]) {
     const uint2 v = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    const float2 a = bf16x2_to_float2(v.x);
+    const float2 b = bf16x2_to_float2(v.y);
     w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
 }
 __device__ __forceinline__ void st4(__nv_bfloat16 *p, const float (&w)[4]) {
@@ -253,8 +253,10 @@ __host__ __device__ constexpr int warp_smem_bytes(int chunk, bool weighted) {
     return (STAGES * STAGE_BYTES + 64 + 2 * chunk * (weighted ? 8 : 4) + 127) / 128 * 128;
 }
 // a lookup whose bag lies outside its run's table (only malformed offsets
-// can make one); unweighted batches mark it in the offset buffer
+// can make one) is marked in the offset buffer; its copy reads a row of
+// zeros (never written, so zero from module load), so it adds nothing
 constexpr uint32_t NO_ROW = 0xFFFFFFFFu;
+static __device__ __align__(128) float g_zero_row[512];   // the widest gradient row
 
 // One chunk of a long run, as the route kernel describes it.
 struct Chunk {
@@ -363,8 +365,8 @@ __device__ __forceinline__ void unpack_w(const uint2 r, float (&w)[4], __half) {
     w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
 }
 __device__ __forceinline__ void unpack_w(const uint2 r, float (&w)[4], __nv_bfloat16) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+    const float2 a = bf16x2_to_float2(r.x);
+    const float2 b = bf16x2_to_float2(r.y);
     w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
 }
 template <typename WT>
@@ -374,12 +376,24 @@ __device__ __forceinline__ void unpack(const typename WRaw<WT>::t r, float (&w)[
 }
 
 // Short runs (SL < sl_threshold): a group of GL lanes owns one run, so a warp
+#ifndef TBE_SHORT_PREFETCH
+#define TBE_SHORT_PREFETCH 1   // load the next run's range and key one iteration ahead
+#endif
+#ifndef TBE_SHORT_MINB
+#define TBE_SHORT_MINB 3       // 256-thread blocks per SM the register budget must allow
+#endif
+// (FP64 accumulators of FP32 tables take twice the registers: two blocks)
+template <typename WT> constexpr int short_min_blocks() { return sizeof(WT) == 4 ? 2 : TBE_SHORT_MINB; }
+#ifndef TBE_SHORT_U
+#define TBE_SHORT_U 0          // gradient rows in flight per run step (0: 2 or 4 by row width)
+#endif
+
 // works on 32/GL runs at once.  Lane gl of a group holds vectors
 // gl + q*GL (q < NV) of the row (float4 of the gradient, 4 weights).  The
 // weight slice and the momentum are loaded before the gather so their
 // latency overlaps it; U gradient rows of the run are in flight per step.
 template <typename WT, int GL, int NV, int U, bool LAY>
-__global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(256, short_min_blocks<WT>()) tbe_bwd_short_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     // LAY: tables or bags with layouts; without, the layout code folds away
     const tbe_table_layout *layout = LAY ? p.layout : nullptr;
@@ -390,15 +404,26 @@ __global__ void __launch_bounds__(256) tbe_bwd_short_kernel(const BwdParams p) {
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int U_runs = p.counters[C_NUM_UNIQUE];
     const int64_t TD = (int64_t)p.T * p.D;
+    // range and key of the group's next run, loaded one iteration ahead so
+    // their latency overlaps the current run's gather
+    int32_t s_n = 0, e_n = 0;
+    int64_t key_n = 0;
+    auto meta = [&](int r) {
+        if (r < U_runs) {
+            s_n = __ldg(p.seg_off + r);
+            e_n = __ldg(p.seg_off + r + 1);
+            key_n = load_key(p, r);
+        }
+    };
+    // (wide lane vectors keep their registers for the gather instead)
+    constexpr bool PF = TBE_SHORT_PREFETCH && NV <= 2;
+    if (PF) meta(warp * GPW + grp);
     for (int rb = warp * GPW; rb < U_runs; rb += nwarps * GPW) {
         const int r = rb + grp;
-        int32_t s = 0, e = 0;
-        int64_t key = 0;
-        if (r < U_runs) {
-            s = __ldg(p.seg_off + r);
-            e = __ldg(p.seg_off + r + 1);
-            key = load_key(p, r);
-        }
+        if (!PF) meta(r);
+        const int32_t s = s_n, e = e_n;
+        const int64_t key = key_n;
+        if (PF) meta(r + nwarps * GPW);
         bool mine = r < U_runs && e - s < p.sl_threshold;
         int t = 0;
         if (layout != nullptr) {   // the run's table decides its class first
@@ -546,13 +571,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             // only malformed (overlapping) offsets can give a bag outside the
             // run's table: such a lookup copies row 0 and adds nothing
             const bool ok = b >= 0 && b < Bt;
-            if constexpr (WGT) {
-                const float x = p.payload_pos && wt ? __ldg(p.psw + v) : 1.f;
-                o[i] = ok ? (uint32_t)((g0 + b * gs) >> 2) : 0u;   // 16-byte units
-                w[i] = ok ? x : 0.f;
-            } else {
-                o[i] = ok ? (uint32_t)((g0 + b * gs) >> 2) : NO_ROW;
-            }
+            o[i] = ok ? (uint32_t)((g0 + b * gs) >> 2) : NO_ROW;   // 16-byte units
+            if constexpr (WGT) w[i] = p.payload_pos && wt ? __ldg(p.psw + v) : 1.f;
         };
 #pragma unroll
         for (int k = 0; k < PV; ++k)
@@ -572,7 +592,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         const uint32_t dst0 = ring0 + st * STAGE_BYTES;
         for (int j = lane; j < rows; j += 32) {
             const uint32_t oj = o[j];
-            bulk_g2s(dst0 + j * row_bytes, G4 + (WGT || oj != NO_ROW ? oj : 0u), row_bytes, bar);
+            bulk_g2s(dst0 + j * row_bytes, oj != NO_ROW ? (const void *)(G4 + oj) : (const void *)g_zero_row,
+                     row_bytes, bar);
         }
         ++gprod;
     };
@@ -612,7 +633,6 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
         const float *w = WGT ? wgt + buf * p.chunk : nullptr;
-        const uint32_t *ob = offb + buf * p.chunk;
         for (int k = 0; k < cur_nst; ++k) {
             const int st = (int)(gcons % STAGES);
             if (!mbar_wait_bounded(bar0 + 8 * st, (phase >> st) & 1u)) {
@@ -633,14 +653,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 #pragma unroll
                     for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * LPR], x);
                 } else {
-                    // a missing row adds zeros (not 0 x its stand-in copy)
-                    const bool ok = ob[k * R + j] != NO_ROW;
 #pragma unroll
-                    for (int q = 0; q < NV; ++q) {
-                        float4 v = src[q * LPR];
-                        if (!ok) v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        acc4(acc[q], v, 1.f);
-                    }
+                    for (int q = 0; q < NV; ++q) acc4(acc[q], src[q * LPR], 1.f);
                 }
             }
             ++gcons;
@@ -1074,23 +1088,17 @@ inline int persistent_grid(const Launch &L, K kernel, size_t smem = 0, int threa
     return L.num_sms * cached_blocks_per_sm(L.dev, (const void *)kernel, threads, smem);
 }
 
-static constexpr bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-#ifndef TBE_SHORT_MAXNV
-#define TBE_SHORT_MAXNV 4   // gradient vectors a lane of the short-run kernel holds per row
-#endif
-// vectors per lane of the short-run kernel: as many as TBE_SHORT_MAXNV (more
-// where a group of at most 32 lanes needs them), with a power-of-two group
-static constexpr bool short_nv_ok(int V, int nv, int cap) {
-    return nv <= cap && V % nv == 0 && pow2(V / nv) && V / nv <= 32;
-}
-static constexpr int short_vectors_per_lane(int V) {
-    return short_nv_ok(V, 4, TBE_SHORT_MAXNV) ? 4
-           : short_nv_ok(V, 3, TBE_SHORT_MAXNV) ? 3
-           : short_nv_ok(V, 2, TBE_SHORT_MAXNV) ? 2
-           : short_nv_ok(V, 1, TBE_SHORT_MAXNV) ? 1
-           : short_nv_ok(V, 4, 4) ? 4 : short_nv_ok(V, 3, 4) ? 3 : short_nv_ok(V, 2, 4) ? 2 : 1;
-}
+// lanes per run of the short-run kernel, for a gradient row of V 16-byte
+// vectors (V a power of two up to 32, or 64, 96, 128): the whole row up to
+// 16 lanes, 16 lanes for 32 vectors, else 32 lanes.  Measured: 4-vector rows
+// (demo workload) 0.195 ms in 4-lane groups vs 0.252 in 2-lane and 0.406 in
+// 1-lane groups; 32-vector rows (large workload) 2.19 ms in 16-lane groups vs
+// 2.62 in 8-lane and 3.00 in 32-lane groups.
+static constexpr int short_group_lanes(int V) { return V <= 16 ? V : V <= 32 ? 16 : 32; }
 
+#ifndef TBE_CHUNK_MAXB
+#define TBE_CHUNK_MAXB 0   // cap on long-run blocks per SM (0: as many as fit)
+#endif
 template <typename WT, int LPR, int NV, bool FUSED>
 inline void chunk_launch(Launch &L, const BwdParams &p) {
     const bool lay = p.layout != nullptr || p.bag_layout != nullptr;
@@ -1102,7 +1110,9 @@ inline void chunk_launch(Launch &L, const BwdParams &p) {
     const size_t csm = (size_t)(CHUNK_THREADS / 32) * warp_smem_bytes(p.chunk, wgt);
     cached_smem_attr(L.dev, (const void *)kc, csm);
     L.before(FUSED ? "tbe_bwd_fused_long" : "tbe_bwd_grad_accum");
-    kc<<<persistent_grid(L, kc, csm, CHUNK_THREADS), CHUNK_THREADS, csm, L.stream>>>(p);
+    int grid = persistent_grid(L, kc, csm, CHUNK_THREADS);
+    if (TBE_CHUNK_MAXB > 0 && grid > L.num_sms * TBE_CHUNK_MAXB) grid = L.num_sms * TBE_CHUNK_MAXB;
+    kc<<<grid, CHUNK_THREADS, csm, L.stream>>>(p);
     L.after();
 }
 
@@ -1130,10 +1140,11 @@ inline void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
     if (!stream) {
         // short runs: GL lanes per run, 4 gradient vectors per lane where the row allows
         constexpr int V = LPR * NV;                       // float4 vectors per gradient row
-        constexpr int SNV = short_vectors_per_lane(V);
-        constexpr int SGL = V / SNV;
-        static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0, "short-run lane groups");
-        constexpr int SU = SNV >= 3 ? 2 : 4;
+        constexpr int SGL = short_group_lanes(V);
+        constexpr int SNV = V / SGL;
+        static_assert(SGL >= 1 && SGL <= 32 && (32 % SGL) == 0 && SNV * SGL == V && SNV <= 4,
+                      "short-run lane groups");
+        constexpr int SU = TBE_SHORT_U > 0 ? TBE_SHORT_U : SNV >= 3 ? 2 : 4;
         auto ks = (p.layout != nullptr || p.bag_layout != nullptr) ? tbe_bwd_short_kernel<WT, SGL, SNV, SU, true>
                                                                    : tbe_bwd_short_kernel<WT, SGL, SNV, SU, false>;
         L.before("tbe_bwd_short_run");

@@ -89,7 +89,7 @@ __device__ __forceinline__ void accum(ACC (&a)[VB / sizeof(WT)], const Vec<VB> &
             if constexpr (std::is_same<WT, __half>::value)
                 f = __half22float2(*reinterpret_cast<const __half2 *>(&x.v[e]));
             else
-                f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.v[e]));
+                f = bf16x2_to_float2(x.v[e]);
             a[2 * e] = fmaf(w, f.x, a[2 * e]);
             a[2 * e + 1] = fmaf(w, f.y, a[2 * e + 1]);
         }

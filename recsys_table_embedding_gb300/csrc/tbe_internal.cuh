@@ -45,6 +45,20 @@ template <> struct WTraits<__nv_bfloat16> {
     static constexpr int VEC = 8;
 };
 
+// Two bf16 values packed in a 32-bit word (element 0 in the low half) as
+// floats.  A bf16 value is the high half of the float with the same value,
+// so widening is a shift or a mask of the bits (exact for every value).
+#ifndef TBE_BF16_WIDEN_BITS
+#define TBE_BF16_WIDEN_BITS 1
+#endif
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+#if TBE_BF16_WIDEN_BITS
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+#else
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+#endif
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
