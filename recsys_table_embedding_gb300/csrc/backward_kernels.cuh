@@ -227,6 +227,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 #endif
 constexpr int STAGES = TBE_BWD_STAGES;
 constexpr int STAGE_BYTES = 4096;
+#ifndef TBE_CHUNK_STAGE_BYTES
+#define TBE_CHUNK_STAGE_BYTES 4096
+#endif
+constexpr int CSTAGE_BYTES = TBE_CHUNK_STAGE_BYTES;   // stage of the long-run ring (>= the widest row)
+static_assert(CSTAGE_BYTES >= 2048 && CSTAGE_BYTES % 2048 == 0, "long-run stages hold whole rows");
 constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;   // 4 warps: four blocks fit an SM at chunk 256
 constexpr int PV = 8;                // payloads a lane prefetches in registers
 
@@ -246,11 +251,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-// shared memory of one warp: STAGES x STAGE_BYTES ring, STAGES mbarriers,
+// shared memory of one warp: STAGES x CSTAGE_BYTES ring, STAGES mbarriers,
 // then two buffers (current and next chunk) of the gradient-row offset and,
 // for weighted batches, the weight of each lookup
 __host__ __device__ constexpr int warp_smem_bytes(int chunk, bool weighted) {
-    return (STAGES * STAGE_BYTES + 64 + 2 * chunk * (weighted ? 8 : 4) + 127) / 128 * 128;
+    return (STAGES * CSTAGE_BYTES + 64 + 2 * chunk * (weighted ? 8 : 4) + 127) / 128 * 128;
 }
 // a lookup whose bag lies outside its run's table (only malformed offsets
 // can make one) is marked in the offset buffer; its copy reads a row of
@@ -535,8 +540,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
 
     unsigned char *wsm = smem_raw + (threadIdx.x >> 5) * warp_smem_bytes(p.chunk, WGT);
     const uint32_t ring0 = smem_addr(wsm);
-    const uint32_t bar0 = smem_addr(wsm + STAGES * STAGE_BYTES);
-    uint32_t *offb = reinterpret_cast<uint32_t *>(wsm + STAGES * STAGE_BYTES + 64);  // [2][chunk], 16-B units
+    const uint32_t bar0 = smem_addr(wsm + STAGES * CSTAGE_BYTES);
+    uint32_t *offb = reinterpret_cast<uint32_t *>(wsm + STAGES * CSTAGE_BYTES + 64);  // [2][chunk], 16-B units
     float *wgt = WGT ? reinterpret_cast<float *>(offb + 2 * p.chunk) : nullptr;      // [2][chunk]
     if (lane == 0)
         for (int i = 0; i < STAGES; ++i) bar_init(bar0 + 8 * i, 1);
@@ -544,7 +549,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
     __syncwarp();
 
     const uint32_t row_bytes = (uint32_t)p.D * 4;
-    const int R = STAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
+    const int R = CSTAGE_BYTES / (int)row_bytes;   // rows per stage (D <= 512)
     const float4 *G4 = reinterpret_cast<const float4 *>(p.G);
 
     // payload of lookups [s, s + PV*32) into registers (issued early)
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
         if (lane == 0) bar_arrive_expect_tx(bar, (uint32_t)rows * row_bytes);
         __syncwarp();
         const uint32_t *o = offb + buf * p.chunk + k * R;
-        const uint32_t dst0 = ring0 + st * STAGE_BYTES;
+        const uint32_t dst0 = ring0 + st * CSTAGE_BYTES;
         for (int j = lane; j < rows; j += 32) {
             const uint32_t oj = o[j];
             bulk_g2s(dst0 + j * row_bytes, oj != NO_ROW ? (const void *)(G4 + oj) : (const void *)g_zero_row,
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) tbe_bwd_chunk_kernel(const BwdP
             }
             phase ^= 1u << st;
             const int rows = min(R, cur.e - cur.s - k * R);
-            const unsigned char *sp = wsm + st * STAGE_BYTES;
+            const unsigned char *sp = wsm + st * CSTAGE_BYTES;
             for (int j = sub; j < rows; j += RPI) {
                 const float4 *src = reinterpret_cast<const float4 *>(sp + j * row_bytes) + li;
                 if constexpr (WGT) {

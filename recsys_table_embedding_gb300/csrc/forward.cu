@@ -75,11 +75,32 @@ template <int VB> __device__ __forceinline__ Vec<VB> ldg_vec(const void *p) {
     return r;
 }
 
-// acc[e] += w * element e of the vector (FP64 accumulators for FP32 tables)
-template <typename WT, int VB, typename ACC>
+#ifndef TBE_FWD_MIXED_ADD
+#define TBE_FWD_MIXED_ADD 1
+#endif
+// a += element 0, b += element 1 of two packed 16-bit values: one FP32 add
+// per element that takes the 16-bit operand directly (its widening to FP32
+// is exact, so the sum is the FP32 sum of the widened values)
+template <typename WT> __device__ __forceinline__ void add2(float &a, float &b, uint32_t x) {
+    if constexpr (std::is_same<WT, __half>::value)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(a), "+f"(b) : "r"(x));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(a), "+f"(b) : "r"(x));
+}
+
+// acc[e] += w * element e of the vector (FP64 accumulators for FP32 tables);
+// UNIT: w is 1 (unweighted), so 16-bit elements are added without a multiply
+template <typename WT, int VB, bool UNIT = false, typename ACC>
 __device__ __forceinline__ void accum(ACC (&a)[VB / sizeof(WT)], const Vec<VB> &x, float w) {
     constexpr int NW = VB / 4;
-    if constexpr (sizeof(WT) == 4) {
+    if constexpr (sizeof(WT) == 2 && UNIT && TBE_FWD_MIXED_ADD) {
+#pragma unroll
+        for (int e = 0; e < NW; ++e) add2<WT>(a[2 * e], a[2 * e + 1], x.v[e]);
+    } else if constexpr (sizeof(WT) == 4) {
 #pragma unroll
         for (int e = 0; e < NW; ++e) a[e] = fma((double)w, (double)__uint_as_float(x.v[e]), a[e]);
     } else {
@@ -236,7 +257,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
 #pragma unroll
                     for (int u = 0; u < U; ++u)
 #pragma unroll
-                        for (int q = 0; q < NV; ++q) accum<WT, VB>(acc[q], v[u][q], wv[u]);
+                        for (int q = 0; q < NV; ++q) accum<WT, VB, !WEIGHTED>(acc[q], v[u][q], wv[u]);
                 }
             }
             // the rest, one 32/LPR-row step at a time
@@ -251,7 +272,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
 #pragma unroll
                     for (int q = 0; q < NV; ++q) v[q] = ldg_vec<VB>(r + q * LPR * VEC);
 #pragma unroll
-                    for (int q = 0; q < NV; ++q) accum<WT, VB>(acc[q], v[q], wk);
+                    for (int q = 0; q < NV; ++q) accum<WT, VB, !WEIGHTED>(acc[q], v[q], wk);
                 }
             }
         }

@@ -205,6 +205,7 @@ radix_onesweep_kernel(const KeyT *__restrict__ keys_in, const uint32_t *__restri
     for (int i = 0; i < IPT; ++i) {
         const int64_t pos = tile_base + warp * 32 * IPT + i * 32 + lane;
         const uint32_t d = pos < N ? (uint32_t)((k[i] >> shift) & mask) : RADIX;   // RADIX = padding
+        // (per-bit ballots instead measured 0.625 vs 0.552 ms per pass)
         const unsigned peers = __match_any_sync(FULL, d);
         const int leader = __ffs(peers) - 1;
         uint32_t base = 0;
