@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(HF_THREADS) tbe_hist_fwd_kernel(const HistFwdP
         // count the tile's lookups: a warp takes CB bags at a time and its
         // lanes read CU*32 consecutive lookups of each (CB*CU loads in flight
         // per lane); every lookup adds one to its bag's 16-bit row counter
+        // (16-byte vector reads of the indices measured slower: 1.29 vs
+        // 1.00 ms on the histogram workload)
         {
             constexpr int CB = TBE_HIST_CB, CU = TBE_HIST_CU;
             constexpr int NW = HF_THREADS / 32;

@@ -200,9 +200,16 @@ def shaped(wl) -> bool:
     return wl.table_dims is not None or wl.table_dtypes is not None
 
 
-def device_batch(wl, device="cuda"):
+def device_batch(wl, device="cuda", unaligned_indices=False):
+    """The workload's batch on the device; unaligned_indices places the
+    indices one element past a 16-byte boundary."""
     from recsys_table_embedding_gb300 import Batch
     idx = torch.from_numpy(wl.indices).to(device)
+    if unaligned_indices:
+        buf = torch.empty(idx.numel() + 1, dtype=idx.dtype, device=device)
+        buf[1:].copy_(idx)
+        idx = buf[1:]
+        assert idx.data_ptr() % 16 != 0
     off = torch.from_numpy(wl.offsets).to(device)
     psw = torch.from_numpy(wl.per_sample_weights).to(device) if wl.per_sample_weights is not None else None
     wt = torch.from_numpy(wl.weighted_tables).to(device) if wl.weighted_tables is not None else None
@@ -234,7 +241,7 @@ def table_out(wl, out: np.ndarray, t: int) -> np.ndarray:
 
 
 def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
-             preprocess_in_forward=True, device="cuda", meta_fill=None):
+             preprocess_in_forward=True, device="cuda", meta_fill=None, unaligned_indices=False):
     """One forward + backward through the C ABI.  Returns a dict of host arrays.
     meta_fill (a byte value) fills the metadata buffer before the first call,
     in place of whatever a fresh device allocation holds."""
@@ -245,7 +252,7 @@ def run_cuda(wl, W0: torch.Tensor, G: np.ndarray, m0: np.ndarray, cfg=None,
     else:
         W = W0.to(device).contiguous()
         tables = Tables(W, wl.table_offset)
-    batch = device_batch(wl, device)
+    batch = device_batch(wl, device, unaligned_indices)
     tbe = TBE(tables, batch, cfg, preprocess_in_forward=preprocess_in_forward)
     if meta_fill is not None:
         tbe.meta_buf.fill_(meta_fill)

@@ -28,9 +28,10 @@ def _saved_counts(res, wl):
     return h.astype(np.int64).reshape(wl.T, wl.B, 64)
 
 
-def _run(wl, cfg=None, flags=0):
+def _run(wl, cfg=None, flags=0, unaligned_indices=False):
     W0, G, m0 = wl.weights(), wl.grad_out(), _m0(wl)
-    res = run_cuda(wl, W0, G, m0, cfg=cfg, preprocess_in_forward=False)
+    res = run_cuda(wl, W0, G, m0, cfg=cfg, preprocess_in_forward=False,
+                   unaligned_indices=unaligned_indices)
     assert res["path"] == 2
     check_full(wl, W0, G, m0, res)
     np.testing.assert_array_equal(_saved_counts(res, wl), oracle.histogram(wl))
@@ -56,6 +57,28 @@ def test_hist_many_tiles_per_cta_and_k_steps_per_slice():
                                  dtype="f16", B=60000, lengths=("poisson", 16.0),
                                  dist=("uniform",), seed=8)
     _run(wl, cfg=_force())
+
+
+def _ragged_end(wl):
+    """Drop lookups from the last bag until N is not a multiple of 4."""
+    while wl.N % 4 == 0:
+        wl.indices = wl.indices[:-1]
+        wl.offsets = wl.offsets.copy()
+        wl.offsets[-1] -= 1
+    assert wl.offsets[-2] < wl.offsets[-1]
+    return wl
+
+
+@pytest.mark.parametrize("itype", ["int32", "int64"])
+@pytest.mark.parametrize("unaligned", [False, True])
+def test_hist_index_types_and_alignment(itype, unaligned):
+    # int32 and int64 indices and offsets, indices at a 16-byte boundary or
+    # one element past it, a last bag that ends on a ragged element count
+    wl = workloads.make_workload("hidx", T=3, table_rows=[64, 37, 64], D=128, dtype="f16", B=700,
+                                 lengths=("poisson", 70.0), dist=("uniform",), seed=21)
+    wl.indices = wl.indices.astype(itype)
+    wl.offsets = wl.offsets.astype(itype)
+    _run(_ragged_end(wl), cfg=_force(), unaligned_indices=unaligned)
 
 
 @pytest.mark.parametrize("D", [64, 96, 128])
