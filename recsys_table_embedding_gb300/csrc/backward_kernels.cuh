@@ -188,10 +188,10 @@ template <typename ACC> __device__ __forceinline__ ACC *part_of(void *partials, 
     return reinterpret_cast<ACC *>(reinterpret_cast<char *>(partials) + slot * stride);
 }
 
-template <bool L2ONLY, typename ACC, int LPR, int NV>
+// (PB only sets how many loads are in flight, not the order of the additions)
+template <bool L2ONLY, typename ACC, int LPR, int NV, int PB = (NV >= 2 ? 2 : 4)>
 __device__ __forceinline__ void sum_partials(ACC (&acc)[NV][4], void *partials, int64_t stride, int cb,
                                              int nch, int li) {
-    constexpr int PB = NV >= 2 ? 2 : 4;
     for (int c0 = 0; c0 < nch; c0 += PB) {
         ACC v[PB][NV][4];
 #pragma unroll
@@ -1111,6 +1111,7 @@ __global__ void __launch_bounds__(256) tbe_bwd_apply_kernel(const BwdParams p) {
         for (int q = 0; q < NV; ++q)
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[q][x] = ACC(0);
+        // (16 partial rows in flight instead of 4 measured the same)
         if (sub == 0) sum_partials<false, ACC, LPR, NV>(acc, p.partials, p.part_stride, cb, nch, li);
         adagrad_apply<WT, ACC, LPR, NV>(acc, p, p.layout, t, key, lane, sub, li);
     }

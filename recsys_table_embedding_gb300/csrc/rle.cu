@@ -107,21 +107,34 @@ __global__ void __launch_bounds__(RLE_THREADS) rle_count_kernel(const KeyT *__re
 }
 
 // One CTA of 1024 threads: exclusive scan of the tile head counts in place.
+// Exclusive scan of the tile head counts in place, SCAN_PT consecutive
+// counts per thread per round (one round up to 16K tiles: 64M keys).
+constexpr int SCAN_PT = 16;
 __global__ void __launch_bounds__(1024) rle_scan_kernel(int32_t *tile_heads, int64_t ntiles,
                                                         int32_t *counters) {
     __shared__ int tot[32];
     __shared__ int carry;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
-    for (int64_t b0 = 0; b0 < ntiles; b0 += 1024) {
-        const int64_t i = b0 + threadIdx.x;
-        const int x = i < ntiles ? tile_heads[i] : 0;
+    for (int64_t b0 = 0; b0 < ntiles; b0 += 1024 * SCAN_PT) {
+        const int64_t i0 = b0 + (int64_t)threadIdx.x * SCAN_PT;
+        int x[SCAN_PT];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < SCAN_PT; ++j) {
+            x[j] = i0 + j < ntiles ? tile_heads[i0 + j] : 0;
+            sum += x[j];
+        }
         int total;
-        const int ex = block_excl_scan(x, tot, total);
-        const int c = carry;
-        if (i < ntiles) tile_heads[i] = c + ex;
+        const int ex = block_excl_scan(sum, tot, total);
+        int run = carry + ex;
+#pragma unroll
+        for (int j = 0; j < SCAN_PT; ++j) {
+            if (i0 + j < ntiles) tile_heads[i0 + j] = run;
+            run += x[j];
+        }
         __syncthreads();
-        if (threadIdx.x == 0) carry = c + total;
+        if (threadIdx.x == 0) carry += total;
         __syncthreads();
     }
     if (threadIdx.x == 0) counters[C_NUM_UNIQUE] = carry;
