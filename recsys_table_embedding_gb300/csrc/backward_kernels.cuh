@@ -235,7 +235,9 @@ constexpr int STAGE_BYTES = 4096;
 #endif
 constexpr int CSTAGE_BYTES = TBE_CHUNK_STAGE_BYTES;   // stage of the long-run ring (>= the widest row)
 static_assert(CSTAGE_BYTES >= 2048 && CSTAGE_BYTES % 2048 == 0, "long-run stages hold whole rows");
-constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;   // 4 warps: four blocks fit an SM at chunk 256
+// 4 warps: at chunk 256, five blocks fit an SM for unweighted batches, four
+// with the weight buffer
+constexpr int CHUNK_THREADS = TBE_CHUNK_THREADS;
 constexpr int PV = 8;                // payloads a lane prefetches in registers
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
@@ -1134,7 +1136,7 @@ inline int persistent_grid(const Launch &L, K kernel, size_t smem = 0, int threa
 static constexpr int short_group_lanes(int V) { return V <= 16 ? V : V <= 32 ? 16 : 32; }
 
 #ifndef TBE_CHUNK_MAXB
-#define TBE_CHUNK_MAXB 0   // cap on long-run blocks per SM (0: as many as fit)
+#define TBE_CHUNK_MAXB 0   // cap on long-run blocks per SM (0: as many as fit; a cap of 4: 3.64 vs 3.30 ms)
 #endif
 template <typename WT, int LPR, int NV, bool FUSED>
 inline void chunk_launch(Launch &L, const BwdParams &p) {
