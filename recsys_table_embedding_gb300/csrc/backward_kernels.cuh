@@ -393,9 +393,12 @@ __device__ __forceinline__ void unpack(const typename WRaw<WT>::t r, float (&w)[
 #define TBE_SHORT_MINB 3       // 256-thread blocks per SM the register budget must allow
 #endif
 // (FP64 accumulators of FP32 tables take twice the registers: two blocks)
+#ifndef TBE_SHORT_THREADS
+#define TBE_SHORT_THREADS 256   // threads of a short-run block (128, 7 per SM at 72 registers: 2.21 vs 2.19 ms)
+#endif
 template <typename WT> constexpr int short_min_blocks() { return sizeof(WT) == 4 ? 2 : TBE_SHORT_MINB; }
 #ifndef TBE_SHORT_U
-#define TBE_SHORT_U 0          // gradient rows in flight per run step (0: 2 or 4 by row width)
+#define TBE_SHORT_U 0          // gradient rows in flight per run step (0: 2 or 4 by row width; 6 or 8 at two blocks per SM: 3.3-3.5 ms)
 #endif
 
 // works on 32/GL runs at once.  Lane gl of a group holds vectors
@@ -403,7 +406,7 @@ template <typename WT> constexpr int short_min_blocks() { return sizeof(WT) == 4
 // weight slice and the momentum are loaded before the gather so their
 // latency overlaps it; U gradient rows of the run are in flight per step.
 template <typename WT, int GL, int NV, int U, bool LAY>
-__global__ void __launch_bounds__(256, short_min_blocks<WT>()) tbe_bwd_short_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(TBE_SHORT_THREADS, short_min_blocks<WT>()) tbe_bwd_short_kernel(const BwdParams p) {
     using ACC = typename WTraits<WT>::acc;
     // LAY: tables or bags with layouts; without, the layout code folds away
     const tbe_table_layout *layout = LAY ? p.layout : nullptr;
@@ -1187,7 +1190,7 @@ inline void bwd_launch(Launch &L, const BwdParams &p, int long_mode) {
         auto ks = (p.layout != nullptr || p.bag_layout != nullptr) ? tbe_bwd_short_kernel<WT, SGL, SNV, SU, true>
                                                                    : tbe_bwd_short_kernel<WT, SGL, SNV, SU, false>;
         L.before("tbe_bwd_short_run");
-        ks<<<persistent_grid(L, ks), 256, 0, L.stream>>>(p);
+        ks<<<persistent_grid(L, ks, 0, TBE_SHORT_THREADS), TBE_SHORT_THREADS, 0, L.stream>>>(p);
         L.after();
     }
     if (long_mode == TBE_LONG_TWO_KERNEL) {
