@@ -300,6 +300,16 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
     if (lane == 0 && oob) atomicAdd(p.status, oob);
 }
 
+// 256-thread blocks per SM the register budget must allow.  Large workload:
+// 8 (32 registers, a few spilled, a full SM of warps) 2.05 ms; without a
+// bound the compiler's 40 registers 2.20 ms; 5 blocks 2.35 ms.  (The next
+// round's index loaded with the current round's: 2.31.)
+#ifndef TBE_FWD_GROUP_MINB
+#define TBE_FWD_GROUP_MINB 8
+#endif
+// (with layouts, whose code needs more registers, 6 blocks: 40 registers)
+template <bool LAY> constexpr int fwd_group_minb() { return LAY ? 6 : TBE_FWD_GROUP_MINB; }
+
 // Rows of at most 16 lanes: one bag per group of LPR lanes, 32/LPR bags per
 // warp.  Each warp instruction then serves several bags, so the per-bag work
 // (offsets, table bounds, index and key traffic, output store) is shared,
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(256) tbe_fwd_kernel(const __grid_constant__ Fw
 // together, U rows per step without predicates while every group has that
 // many valid lookups left, then one row per step with a per-group check.
 template <typename WT, int VB, int LPR, int NV, int U, bool WEIGHTED, typename IdxT, bool LAY>
-__global__ void __launch_bounds__(256) tbe_fwd_group_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(256, fwd_group_minb<LAY>()) tbe_fwd_group_kernel(const __grid_constant__ FwdParams p) {
     static_assert(LPR <= 16, "groups of at most half a warp");
     const int ntl = LAY ? p.ntl : 0;
     const tbe_table_layout *layout = LAY ? p.layout : nullptr;
